@@ -1,0 +1,248 @@
+"""CPU oracle for the top-k routed MoE SwiGLU FFN layer (forward pass).
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg, never by the CUDA path.  The arithmetic lives in
+``moe_oracle.c`` (plain C loops, fp32 router, fp64 experts); this file only
+marshals numpy arrays into it.  Every function cites the page passage it
+follows in the C source.  Parity pins for each function are in
+``tests/test_oracle_*.py``; none of them is unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# A prebuilt copy may be substituted (the mutation test loads planted-mistake builds this way).
+_OVERRIDE = os.environ.get("MOE_ORACLE_LIB")
+_lib = None
+
+F32, BF16 = 0, 1
+TIE_EPS = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so with gcc (OpenMP over tokens)."""
+    if _OVERRIDE:
+        return _OVERRIDE
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        L.oracle_round_bf16.argtypes = [D]
+        L.oracle_round_bf16.restype = ctypes.c_uint16
+        L.oracle_route.argtypes = [I64, I32, I32, I32, I32, P, P, P, I32, P, P, P, P]
+        L.oracle_capacity.argtypes = [I64, I32, I32, D]
+        L.oracle_capacity.restype = I64
+        L.oracle_permute.argtypes = [I64, I32, I32, P, I64, P, P, P, P, P, P]
+        L.oracle_keep_naive.argtypes = [I64, I32, I32, P, I64, P]
+        L.oracle_keep_naive.restype = None
+        L.oracle_moe_token.argtypes = [I32, I32, I32, I32, I32, I32, I32, P, P, P,
+                                       P, P, P, P, P, P, P]
+        L.oracle_forward_naive.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
+                                           P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
+        L.oracle_forward_grouped.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
+                                             P, P, P, P, P, P, P, P, P, P]
+        L.oracle_stats.argtypes = [I64, I32, I32, P, P, P, P, D, P, P, P, P]
+        for fn in ("oracle_route", "oracle_permute", "oracle_moe_token", "oracle_forward_naive",
+                   "oracle_forward_grouped", "oracle_stats"):
+            getattr(L, fn).restype = I32
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def as_host(a, dtype_code: int) -> np.ndarray:
+    """torch tensor / numpy array -> contiguous numpy (bf16 as uint16 bits)."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                return a.view(torch.int16).numpy().view(np.uint16)
+            return a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if dtype_code == BF16 and a.dtype != np.uint16:
+        raise TypeError("bf16 arrays are passed as uint16 bit patterns")
+    return a
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def round_bf16(v: float) -> int:
+    return int(lib().oracle_round_bf16(float(v)))
+
+
+def capacity(N: int, k: int, E: int, cf: float) -> int:
+    return int(lib().oracle_capacity(N, k, E, float(cf)))
+
+
+# ---------------------------------------------------------------- steps
+
+def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1):
+    """Router: returns idx [N,k] int32, w [N,k] f32, probs [N,E] f32, gap [N] f32."""
+    x = as_host(x, dtype)
+    W_r = np.ascontiguousarray(as_host(W_r, F32), dtype=np.float32)
+    b = None if b_r is None else np.ascontiguousarray(as_host(b_r, F32), dtype=np.float32)
+    N, d = x.shape
+    E = W_r.shape[0]
+    idx = np.zeros((N, k), np.int32)
+    w = np.zeros((N, k), np.float32)
+    probs = np.zeros((N, E), np.float32)
+    gap = np.zeros((N,), np.float32)
+    rc = lib().oracle_route(N, d, E, k, dtype, _p(x), _p(W_r), _p(b), renorm,
+                            _p(idx), _p(w), _p(probs), _p(gap))
+    if rc:
+        raise ValueError("oracle_route rejected its arguments")
+    return idx, w, probs, gap
+
+
+def permute(idx: np.ndarray, E: int, cap: int = -1):
+    """Grouping by expert: counts, offsets, kept, kept_offsets, perm, pos."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    N, k = idx.shape
+    A = N * k
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    kept = np.zeros(E, np.int32)
+    kept_offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(max(A, 1), np.int32)
+    pos = np.zeros(max(A, 1), np.int32)
+    rc = lib().oracle_permute(N, k, E, _p(idx), cap, _p(counts), _p(offsets), _p(kept),
+                              _p(kept_offsets), _p(perm), _p(pos))
+    if rc:
+        raise ValueError("oracle_permute: expert index out of range")
+    return dict(counts=counts, offsets=offsets, kept=kept, kept_offsets=kept_offsets,
+                perm=perm[:A], pos=pos[:A])
+
+
+def keep_naive(idx: np.ndarray, E: int, cap: int) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    N, k = idx.shape
+    keep = np.zeros((N, k), np.int32)
+    lib().oracle_keep_naive(N, k, E, _p(idx), cap, _p(keep))
+    return keep
+
+
+def moe_token(x_t, w_t, keep_t, experts: Sequence, shared: Sequence, dtype: int,
+              round_h: int) -> np.ndarray:
+    """One token's layer output.  experts: k tuples (Wg [F,d], Wu [F,d], Wd [d,F]) of the
+    chosen experts in slot order; shared: S such tuples.  Arrays in the layer dtype."""
+    x_t = as_host(x_t, dtype)
+    d = x_t.shape[-1]
+    k, S = len(experts), len(shared)
+    mats = [[as_host(m, dtype) for m in trip] for trip in experts]
+    smats = [[as_host(m, dtype) for m in trip] for trip in shared]
+    F = mats[0][0].shape[0] if k else 0
+    Fs = smats[0][0].shape[0] if S else 0
+
+    def ptrs(ms, i):
+        arr = (ctypes.c_void_p * max(len(ms), 1))()
+        for j, trip in enumerate(ms):
+            arr[j] = trip[i].ctypes.data
+        return arr
+
+    w_t = np.ascontiguousarray(w_t, dtype=np.float32)
+    keep_t = np.ascontiguousarray(keep_t, dtype=np.int32)
+    out = np.zeros(d, np.uint16 if dtype == BF16 else np.float32)
+    rc = lib().oracle_moe_token(d, F, k, S, Fs, dtype, round_h, _p(x_t), _p(w_t), _p(keep_t),
+                                ptrs(mats, 0), ptrs(mats, 1), ptrs(mats, 2),
+                                ptrs(smats, 0), ptrs(smats, 1), ptrs(smats, 2), _p(out))
+    if rc:
+        raise ValueError("oracle_moe_token rejected its arguments")
+    return out
+
+
+def _layer_arrays(layer, dtype):
+    g = lambda n: None if layer.get(n) is None else as_host(layer[n], dtype)
+    x = as_host(layer["x"], dtype)
+    W_r = np.ascontiguousarray(as_host(layer["W_r"], F32), dtype=np.float32)
+    b_r = None if layer.get("b_r") is None else np.ascontiguousarray(as_host(layer["b_r"], F32),
+                                                                     dtype=np.float32)
+    return x, W_r, b_r, g("W_gate"), g("W_up"), g("W_down"), g("Ws_gate"), g("Ws_up"), g("Ws_down")
+
+
+def forward_naive(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int = 1,
+                  round_h: Optional[int] = None):
+    """The whole layer token by token.  Returns (out, extras dict)."""
+    x, W_r, b_r, Wg, Wu, Wd, Wsg, Wsu, Wsd = _layer_arrays(layer, dtype)
+    round_h = (1 if dtype == BF16 else 0) if round_h is None else round_h
+    N, d = x.shape
+    E, F = Wg.shape[0], Wg.shape[1]
+    S = 0 if Wsg is None else Wsg.shape[0]
+    Fs = 0 if Wsg is None else Wsg.shape[1]
+    out = np.zeros_like(x)
+    idx = np.zeros((N, k), np.int32)
+    w = np.zeros((N, k), np.float32)
+    keep = np.zeros((N, k), np.int32)
+    probs = np.zeros((N, E), np.float32)
+    gap = np.zeros((N,), np.float32)
+    rc = lib().oracle_forward_naive(N, d, F, E, k, S, Fs, dtype, float(cf), renorm, round_h,
+                                    _p(x), _p(W_r), _p(b_r), _p(Wg), _p(Wu), _p(Wd),
+                                    _p(Wsg), _p(Wsu), _p(Wsd), _p(out), _p(idx), _p(w),
+                                    _p(keep), _p(probs), _p(gap))
+    if rc:
+        raise ValueError("oracle_forward_naive rejected its arguments")
+    return out, dict(idx=idx, w=w, keep=keep, probs=probs, gap=gap)
+
+
+def forward_grouped(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int = 1,
+                    round_h: Optional[int] = None):
+    x, W_r, b_r, Wg, Wu, Wd, Wsg, Wsu, Wsd = _layer_arrays(layer, dtype)
+    round_h = (1 if dtype == BF16 else 0) if round_h is None else round_h
+    N, d = x.shape
+    E, F = Wg.shape[0], Wg.shape[1]
+    S = 0 if Wsg is None else Wsg.shape[0]
+    Fs = 0 if Wsg is None else Wsg.shape[1]
+    out = np.zeros_like(x)
+    rc = lib().oracle_forward_grouped(N, d, F, E, k, S, Fs, dtype, float(cf), renorm, round_h,
+                                      _p(x), _p(W_r), _p(b_r), _p(Wg), _p(Wu), _p(Wd),
+                                      _p(Wsg), _p(Wsu), _p(Wsd), _p(out))
+    if rc:
+        raise ValueError("oracle_forward_grouped rejected its arguments")
+    return out
+
+
+def stats(idx: np.ndarray, probs: np.ndarray, keep: Optional[np.ndarray] = None,
+          gap: Optional[np.ndarray] = None, tie_eps: float = TIE_EPS):
+    """Load-balance statistics: f [E], P [E], aux, dropped, fully_dropped, near_tie."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    probs = np.ascontiguousarray(probs, dtype=np.float32)
+    N, k = idx.shape
+    E = probs.shape[1]
+    keep = None if keep is None else np.ascontiguousarray(keep, dtype=np.int32)
+    gap = None if gap is None else np.ascontiguousarray(gap, dtype=np.float32)
+    f = np.zeros(E, np.float64)
+    P = np.zeros(E, np.float64)
+    aux = ctypes.c_double(0.0)
+    cnt = np.zeros(3, np.int64)
+    rc = lib().oracle_stats(N, E, k, _p(idx), _p(probs), _p(keep), _p(gap), tie_eps,
+                            _p(f), _p(P), ctypes.byref(aux), _p(cnt))
+    if rc:
+        raise ValueError("oracle_stats rejected its arguments")
+    return dict(f=f, P=P, aux=aux.value, dropped=int(cnt[0]), fully_dropped=int(cnt[1]),
+                near_tie=int(cnt[2]))

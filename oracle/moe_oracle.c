@@ -1,0 +1,502 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for the forward pass of a top-k routed
+ * Mixture-of-Experts SwiGLU FFN layer with optional shared experts.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * Sources (pages of the subject, cited by title and section):
+ *   [H]  "混合专家 MoE" (ai-infra-handbooks, Transformer 解剖), sections
+ *        "结构", "实现：逐 token 与按专家分组" (listing moe.py: Expert, MoE.route,
+ *        forward_naive, forward_grouped), "负载均衡" (aux_loss listing),
+ *        "练习" (exercise 1 parameter count).
+ *   [N]  "混合专家模型 (MoE)：大规模稀疏条件计算的架构与工程实践", section
+ *        三.1 "容量因子 (Capacity Factor) 与 Token 丢弃策略" and 一.1 (shared
+ *        experts always active).
+ *
+ * Precision.  The router is fp32 as the layer definition fixes it: each logit
+ * is the fp32 rounding of the exact dot product (accumulated in fp64 from the
+ * exact fp32 x fp32 products), the softmax is evaluated in fp64 and each
+ * probability rounded once to fp32; top-k and the near-tie gap are decided on
+ * those fp32 probabilities.  Everything in the expert FFNs is fp64; for bf16
+ * layers the SwiGLU hidden vector h is rounded to bf16 before the down
+ * projection (the single intermediate rounding point of the bf16 path) and the
+ * output is rounded once to bf16.  bf16 inputs are widened exactly.
+ *
+ * Readings where the pages are silent:
+ *   - top-k orders slots by probability descending, ties to the lower index;
+ *   - capacity C = ceil(CF * N * k / E); an expert keeps the first C of its
+ *     assignments in (token, slot) order; a dropped assignment contributes 0
+ *     and the remaining weights are not renormalised; shared experts still
+ *     apply to every token;
+ *   - f_i = (assignments to expert i before dropping) / (N * k),
+ *     P_i = mean over tokens of the router probability of expert i.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* ---------- scalar conversions ---------- */
+
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 value, ties to even (bf16: 8 significant
+ * bits, 8 exponent bits, subnormal quantum 2^-133).  Returns the bf16 bits. */
+uint16_t oracle_round_bf16(double v)
+{
+    double r;
+    if (isnan(v))
+        return (uint16_t)0x7FC0;
+    if (v == 0.0 || isinf(v)) {
+        r = v;
+    } else if (fabs(v) < ldexp(1.0, -126)) {
+        r = ldexp(nearbyint(ldexp(v, 133)), -133);
+    } else {
+        int e;
+        double m = frexp(v, &e);            /* v = m * 2^e, 0.5 <= |m| < 1 */
+        r = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    }
+    /* largest finite bf16 is (2 - 2^-7) * 2^127 */
+    if (fabs(r) > ldexp(255.0, 120))
+        r = copysign(INFINITY, r);
+    float f = (float)r;                     /* exact: r is a bf16 value */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+static double round_to_bf16_value(double v)
+{
+    return bf16_bits_to_double(oracle_round_bf16(v));
+}
+
+/* element i of a matrix stored as fp32 or bf16 */
+static double elem(const void *p, int dtype, int64_t i)
+{
+    if (dtype == ORC_BF16)
+        return bf16_bits_to_double(((const uint16_t *)p)[i]);
+    return (double)((const float *)p)[i];
+}
+
+/* ---------- router: logits, softmax, top-k, renormalise ([H] MoE.route) ---------- */
+
+/* For one token: probs[E] (fp32), idx[k], w[k], gap.  Returns 0. */
+static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t,
+                        const float *W_r, const float *b_r, int renorm,
+                        float *probs, int32_t *idx, float *w, float *gap)
+{
+    float *logit = (float *)malloc(sizeof(float) * (size_t)E);
+    unsigned char *chosen = (unsigned char *)calloc((size_t)E, 1);
+
+    /* logits: l[e] = b_e + sum_i x[t,i] * W_r[e,i], rounded once to fp32 */
+    for (int e = 0; e < E; e++) {
+        double acc = b_r ? (double)b_r[e] : 0.0;
+        for (int i = 0; i < d; i++)
+            acc += elem(x, dtype, t * (int64_t)d + i) * (double)W_r[(int64_t)e * d + i];
+        logit[e] = (float)acc;
+    }
+
+    /* softmax over all E experts, with the maximum subtracted */
+    double mx = logit[0];
+    for (int e = 1; e < E; e++)
+        if (logit[e] > mx)
+            mx = logit[e];
+    double s = 0.0;
+    for (int e = 0; e < E; e++)
+        s += exp((double)logit[e] - mx);
+    for (int e = 0; e < E; e++)
+        probs[e] = (float)(exp((double)logit[e] - mx) / s);
+
+    /* top-k: k rounds of "largest not yet chosen", ties to the lower index */
+    for (int j = 0; j < k; j++) {
+        int best = -1;
+        for (int e = 0; e < E; e++)
+            if (!chosen[e] && (best < 0 || probs[e] > probs[best]))
+                best = e;
+        idx[j] = best;
+        chosen[best] = 1;
+    }
+
+    /* gap between the k-th and the (k+1)-th probability (none when k == E) */
+    if (k < E) {
+        int nb = -1;
+        for (int e = 0; e < E; e++)
+            if (!chosen[e] && (nb < 0 || probs[e] > probs[nb]))
+                nb = e;
+        *gap = (float)((double)probs[idx[k - 1]] - (double)probs[nb]);
+    } else {
+        *gap = INFINITY;
+    }
+
+    /* renormalise the k selected weights so they sum to one */
+    double ws = 0.0;
+    for (int j = 0; j < k; j++)
+        ws += (double)probs[idx[j]];
+    for (int j = 0; j < k; j++)
+        w[j] = renorm ? (float)((double)probs[idx[j]] / ws) : probs[idx[j]];
+
+    free(logit);
+    free(chosen);
+}
+
+/*
+ * oracle_route: router for all N tokens.
+ *   x [N,d] (fp32 or bf16 bits), W_r [E,d] fp32, b_r [E] fp32 or NULL.
+ *   idx [N,k] int32, w [N,k] fp32; probs [N,E] fp32 and gap [N] fp32 may be NULL.
+ */
+int oracle_route(int64_t N, int d, int E, int k, int dtype, const void *x,
+                 const float *W_r, const float *b_r, int renorm,
+                 int32_t *idx, float *w, float *probs, float *gap)
+{
+    if (N < 0 || d <= 0 || E <= 0 || k <= 0 || k > E)
+        return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < N; t++) {
+        float *p = (float *)malloc(sizeof(float) * (size_t)E);
+        float g;
+        route_token(d, E, k, dtype, x, t, W_r, b_r, renorm, p, idx + t * k, w + t * k, &g);
+        if (probs)
+            memcpy(probs + t * (int64_t)E, p, sizeof(float) * (size_t)E);
+        if (gap)
+            gap[t] = g;
+        free(p);
+    }
+    return 0;
+}
+
+/* ---------- capacity ([N] 三.1) ---------- */
+
+/* C = ceil(CF * N * k / E); -1 when CF <= 0 (no limit). */
+int64_t oracle_capacity(int64_t N, int k, int E, double cf)
+{
+    if (!(cf > 0.0))
+        return -1;
+    return (int64_t)ceil(cf * (double)N * (double)k / (double)E);
+}
+
+/* ---------- grouping by expert ([H] forward_grouped: flatten, stable argsort, bincount) ---------- */
+
+/*
+ * oracle_permute: flat slot f = t*k + j goes to expert idx[f].
+ *   counts[E]       = histogram of idx                       (bincount)
+ *   offsets[E+1]    = exclusive prefix sum of counts         (segment starts)
+ *   perm[N*k]       = slots sorted by expert, stable         (argsort(stable=True))
+ *   kept[E]         = min(counts, C)
+ *   kept_offsets[E+1] = exclusive prefix sum of kept
+ *   pos[N*k]        = row of slot f in the compacted kept order, or -1 if dropped
+ * capacity < 0 means no limit.  Returns 1 on an index outside [0, E).
+ */
+int oracle_permute(int64_t N, int k, int E, const int32_t *idx, int64_t capacity,
+                   int32_t *counts, int32_t *offsets, int32_t *kept, int32_t *kept_offsets,
+                   int32_t *perm, int32_t *pos)
+{
+    if (N < 0 || k <= 0 || E <= 0)
+        return 1;
+    int64_t A = N * k;
+    for (int64_t f = 0; f < A; f++)
+        if (idx[f] < 0 || idx[f] >= E)
+            return 1;
+    for (int e = 0; e < E; e++)
+        counts[e] = 0;
+    for (int64_t f = 0; f < A; f++)
+        counts[idx[f]]++;
+    offsets[0] = 0;
+    for (int e = 0; e < E; e++)
+        offsets[e + 1] = offsets[e] + counts[e];
+    kept_offsets[0] = 0;
+    for (int e = 0; e < E; e++) {
+        kept[e] = (capacity >= 0 && counts[e] > capacity) ? (int32_t)capacity : counts[e];
+        kept_offsets[e + 1] = kept_offsets[e] + kept[e];
+    }
+    /* counting sort: walking f in increasing order keeps equal keys stable */
+    int32_t *cursor = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t f = 0; f < A; f++) {
+        int e = idx[f];
+        int32_t r = cursor[e]++;
+        perm[offsets[e] + r] = (int32_t)f;
+        pos[f] = (r < kept[e]) ? kept_offsets[e] + r : -1;
+    }
+    free(cursor);
+    return 0;
+}
+
+/* ---------- one expert on one token ([H] Expert.forward) ---------- */
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* y[d] = W_down (silu(W_gate x) * (W_up x)); W_gate/W_up [F,d], W_down [d,F]. */
+static void swiglu_expert(const double *xt, int d, int F, int dtype, const void *Wg,
+                          const void *Wu, const void *Wd, int round_h, double *y)
+{
+    double *h = (double *)malloc(sizeof(double) * (size_t)F);
+    for (int n = 0; n < F; n++) {
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < d; i++) {
+            g += elem(Wg, dtype, (int64_t)n * d + i) * xt[i];
+            u += elem(Wu, dtype, (int64_t)n * d + i) * xt[i];
+        }
+        double hv = silu(g) * u;
+        h[n] = round_h ? round_to_bf16_value(hv) : hv;
+    }
+    for (int i = 0; i < d; i++) {
+        double acc = 0.0;
+        for (int n = 0; n < F; n++)
+            acc += elem(Wd, dtype, (int64_t)i * F + n) * h[n];
+        y[i] = acc;
+    }
+    free(h);
+}
+
+static void store_row(void *out, int dtype, int64_t row, int d, const double *acc)
+{
+    for (int i = 0; i < d; i++) {
+        if (dtype == ORC_BF16)
+            ((uint16_t *)out)[row * d + i] = oracle_round_bf16(acc[i]);
+        else
+            ((float *)out)[row * d + i] = (float)acc[i];
+    }
+}
+
+/*
+ * oracle_moe_token: the layer output for one token ([H] forward_naive body):
+ *   out_t = sum_{j : keep_t[j]} w_t[j] * Expert_{idx_t[j]}(x_t)  +  sum_s Shared_s(x_t)
+ * The k chosen experts' matrices are passed as pointer arrays (Wg_k[j] is the
+ * [F,d] gate matrix of expert idx_t[j], ...), the S shared experts likewise.
+ * x_t [d] and out_t [d] are in the layer dtype.
+ */
+int oracle_moe_token(int d, int F, int k, int S, int Fs, int dtype, int round_h,
+                     const void *x_t, const float *w_t, const int32_t *keep_t,
+                     const void *const *Wg_k, const void *const *Wu_k, const void *const *Wd_k,
+                     const void *const *Wsg, const void *const *Wsu, const void *const *Wsd,
+                     void *out_t)
+{
+    double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+    double *acc = (double *)calloc((size_t)d, sizeof(double));
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; i++)
+        xt[i] = elem(x_t, dtype, i);
+    for (int j = 0; j < k; j++) {
+        if (!keep_t[j])
+            continue;
+        swiglu_expert(xt, d, F, dtype, Wg_k[j], Wu_k[j], Wd_k[j], round_h, y);
+        for (int i = 0; i < d; i++)
+            acc[i] += (double)w_t[j] * y[i];
+    }
+    for (int s = 0; s < S; s++) {
+        swiglu_expert(xt, d, Fs, dtype, Wsg[s], Wsu[s], Wsd[s], round_h, y);
+        for (int i = 0; i < d; i++)
+            acc[i] += y[i];
+    }
+    store_row(out_t, dtype, 0, d, acc);
+    free(xt);
+    free(acc);
+    free(y);
+    return 0;
+}
+
+static const void *expert_mat(const void *bank, int dtype, int64_t e, int64_t rows, int64_t cols)
+{
+    size_t esz = dtype == ORC_BF16 ? 2 : 4;
+    return (const char *)bank + (size_t)(e * rows * cols) * esz;
+}
+
+/*
+ * oracle_keep_naive: which assignments survive the capacity limit, decided the
+ * per-token way: walking tokens t = 0..N-1 and slots j = 0..k-1, an assignment
+ * to expert e is kept while fewer than C earlier assignments went to e.
+ * keep[N*k] gets 1/0.  capacity < 0: everything kept.
+ */
+void oracle_keep_naive(int64_t N, int k, int E, const int32_t *idx, int64_t capacity, int32_t *keep)
+{
+    int64_t *seen = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    for (int64_t t = 0; t < N; t++)
+        for (int j = 0; j < k; j++) {
+            int e = idx[t * k + j];
+            keep[t * k + j] = (capacity < 0 || seen[e] < capacity) ? 1 : 0;
+            seen[e]++;
+        }
+    free(seen);
+}
+
+/*
+ * oracle_forward_naive: the whole layer, token by token ([H] forward_naive).
+ * Weights: Wg/Wu [E,F,d], Wd [E,d,F], Wsg/Wsu [S,Fs,d], Wsd [S,d,Fs] in the layer
+ * dtype (fp32 or bf16 bits); W_r fp32 [E,d]; b_r fp32 [E] or NULL.
+ * Optional outputs (NULL to skip): idx/w/keep [N,k], probs [N,E], gap [N].
+ */
+int oracle_forward_naive(int64_t N, int d, int F, int E, int k, int S, int Fs, int dtype,
+                         double cf, int renorm, int round_h,
+                         const void *x, const float *W_r, const float *b_r,
+                         const void *Wg, const void *Wu, const void *Wd,
+                         const void *Wsg, const void *Wsu, const void *Wsd,
+                         void *out, int32_t *idx_o, float *w_o, int32_t *keep_o,
+                         float *probs_o, float *gap_o)
+{
+    if (N < 0 || k > E || k <= 0 || k > 64 || S < 0 || S > 64)
+        return 1;
+    int64_t A = N * k;
+    int32_t *idx = idx_o ? idx_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
+    float *w = w_o ? w_o : (float *)malloc(sizeof(float) * (size_t)(A ? A : 1));
+    int32_t *keep = keep_o ? keep_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, renorm, idx, w, probs_o, gap_o);
+    if (rc) {
+        if (!idx_o) free(idx);
+        if (!w_o) free(w);
+        if (!keep_o) free(keep);
+        return rc;
+    }
+    oracle_keep_naive(N, k, E, idx, oracle_capacity(N, k, E, cf), keep);
+    size_t esz = dtype == ORC_BF16 ? 2 : 4;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < N; t++) {
+        const void *gk[64], *uk[64], *dk[64], *sg[64], *su[64], *sd[64];
+        for (int j = 0; j < k; j++) {
+            int e = idx[t * k + j];
+            gk[j] = expert_mat(Wg, dtype, e, F, d);
+            uk[j] = expert_mat(Wu, dtype, e, F, d);
+            dk[j] = expert_mat(Wd, dtype, e, d, F);
+        }
+        for (int s = 0; s < S; s++) {
+            sg[s] = expert_mat(Wsg, dtype, s, Fs, d);
+            su[s] = expert_mat(Wsu, dtype, s, Fs, d);
+            sd[s] = expert_mat(Wsd, dtype, s, d, Fs);
+        }
+        oracle_moe_token(d, F, k, S, Fs, dtype, round_h, (const char *)x + (size_t)(t * d) * esz,
+                         w + t * k, keep + t * k, gk, uk, dk, sg, su, sd,
+                         (char *)out + (size_t)(t * d) * esz);
+    }
+    if (!idx_o) free(idx);
+    if (!w_o) free(w);
+    if (!keep_o) free(keep);
+    return 0;
+}
+
+/*
+ * oracle_forward_grouped: the same layer organised per expert ([H]
+ * forward_grouped): route, stable-sort the slots by expert, then for each
+ * expert run its kept tokens and add w * y back at the token's row; shared
+ * experts on every token last.  Used to check that both organisations agree.
+ */
+int oracle_forward_grouped(int64_t N, int d, int F, int E, int k, int S, int Fs, int dtype,
+                           double cf, int renorm, int round_h,
+                           const void *x, const float *W_r, const float *b_r,
+                           const void *Wg, const void *Wu, const void *Wd,
+                           const void *Wsg, const void *Wsu, const void *Wsd, void *out)
+{
+    if (N < 0 || k > E || k <= 0)
+        return 1;
+    int64_t A = N * k;
+    size_t a1 = (size_t)(A ? A : 1);
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * a1);
+    float *w = (float *)malloc(sizeof(float) * a1);
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * a1);
+    int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * a1);
+    int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *kept = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    int32_t *kept_off = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    double *acc = (double *)calloc((size_t)(N * d ? N * d : 1), sizeof(double));
+    double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, renorm, idx, w, NULL, NULL);
+    if (!rc)
+        rc = oracle_permute(N, k, E, idx, oracle_capacity(N, k, E, cf), counts, offsets, kept,
+                            kept_off, perm, pos);
+    if (!rc) {
+        for (int e = 0; e < E; e++) {
+            for (int32_t r = 0; r < kept[e]; r++) {       /* empty experts are skipped */
+                int32_t f = perm[offsets[e] + r];
+                int64_t t = f / k;
+                for (int i = 0; i < d; i++)
+                    xt[i] = elem(x, dtype, t * d + i);
+                swiglu_expert(xt, d, F, dtype, expert_mat(Wg, dtype, e, F, d),
+                              expert_mat(Wu, dtype, e, F, d), expert_mat(Wd, dtype, e, d, F),
+                              round_h, y);
+                for (int i = 0; i < d; i++)
+                    acc[t * d + i] += (double)w[f] * y[i];
+            }
+        }
+        for (int s = 0; s < S; s++)
+            for (int64_t t = 0; t < N; t++) {
+                for (int i = 0; i < d; i++)
+                    xt[i] = elem(x, dtype, t * d + i);
+                swiglu_expert(xt, d, Fs, dtype, expert_mat(Wsg, dtype, s, Fs, d),
+                              expert_mat(Wsu, dtype, s, Fs, d), expert_mat(Wsd, dtype, s, d, Fs),
+                              round_h, y);
+                for (int i = 0; i < d; i++)
+                    acc[t * d + i] += y[i];
+            }
+        for (int64_t t = 0; t < N; t++)
+            store_row(out, dtype, t, d, acc + t * d);
+    }
+    free(idx); free(w); free(perm); free(pos); free(counts); free(kept);
+    free(offsets); free(kept_off); free(acc); free(xt); free(y);
+    return rc;
+}
+
+/* ---------- load-balance statistics ([H] 负载均衡, aux_loss) ---------- */
+
+/*
+ * oracle_stats:
+ *   f[e] = #{slots routed to e, before dropping} / (N*k)
+ *   P[e] = (1/N) sum_t probs[t,e]
+ *   aux  = E * sum_e f[e] * P[e]
+ *   counters[0] = dropped assignments, [1] = tokens with every assignment dropped,
+ *   counters[2] = tokens whose k-th and (k+1)-th probabilities differ by < tie_eps.
+ * keep [N*k] (NULL = all kept), gap [N] (NULL = no tie count).
+ */
+int oracle_stats(int64_t N, int E, int k, const int32_t *idx, const float *probs,
+                 const int32_t *keep, const float *gap, double tie_eps,
+                 double *f, double *P, double *aux, int64_t *counters)
+{
+    if (N <= 0 || E <= 0 || k <= 0)
+        return 1;
+    for (int e = 0; e < E; e++) {
+        f[e] = 0.0;
+        P[e] = 0.0;
+    }
+    for (int64_t s = 0; s < N * k; s++) {
+        if (idx[s] < 0 || idx[s] >= E)
+            return 1;
+        f[idx[s]] += 1.0;
+    }
+    for (int e = 0; e < E; e++)
+        f[e] /= (double)(N * k);
+    for (int e = 0; e < E; e++) {
+        double s = 0.0;
+        for (int64_t t = 0; t < N; t++)
+            s += (double)probs[t * E + e];
+        P[e] = s / (double)N;
+    }
+    double a = 0.0;
+    for (int e = 0; e < E; e++)
+        a += f[e] * P[e];
+    *aux = (double)E * a;
+    counters[0] = counters[1] = counters[2] = 0;
+    for (int64_t t = 0; t < N; t++) {
+        int any = 0;
+        for (int j = 0; j < k; j++) {
+            int kp = keep ? keep[t * k + j] : 1;
+            if (!kp)
+                counters[0]++;
+            any |= kp;
+        }
+        if (!any)
+            counters[1]++;
+        if (gap && (double)gap[t] < tie_eps)
+            counters[2]++;
+    }
+    return 0;
+}

@@ -1,0 +1,68 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle's C source
+(never in the real one), builds it on the CPU, and runs the oracle pin suite
+against that build in a subprocess: the suite must fail.  The mistakes are the
+kinds a hand-written oracle can plausibly contain: a dropped term, a wrong
+sign, a transposed operand, a wrong index, a broken tie-break or stability
+rule, an off-by-one in the capacity rule, a wrong normaliser.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "drop_shared_term": ("            acc[i] += y[i];\n    }\n    store_row(out_t",
+                         "            acc[i] += 0.0 * y[i];\n    }\n    store_row(out_t"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "down_transposed": ("elem(Wd, dtype, (int64_t)i * F + n)", "elem(Wd, dtype, (int64_t)n * d + i)"),
+    "gate_up_swapped": ("double hv = silu(g) * u;", "double hv = silu(u) * g;"),
+    "wrong_slot_weight": ("acc[i] += (double)w_t[j] * y[i];", "acc[i] += (double)w_t[0] * y[i];"),
+    "ties_to_higher_index": ("if (!chosen[e] && (best < 0 || probs[e] > probs[best]))",
+                             "if (!chosen[e] && (best < 0 || probs[e] >= probs[best]))"),
+    "no_renorm": ("w[j] = renorm ? (float)((double)probs[idx[j]] / ws) : probs[idx[j]];",
+                  "w[j] = probs[idx[j]];"),
+    "unstable_segments": ("perm[offsets[e] + r] = (int32_t)f;",
+                          "perm[offsets[e + 1] - 1 - r] = (int32_t)f;"),
+    "capacity_off_by_one": ("pos[f] = (r < kept[e]) ? kept_offsets[e] + r : -1;",
+                            "pos[f] = (r <= kept[e] && r < counts[e] - 1) ? kept_offsets[e] + r : -1;"),
+    "f_over_N": ("f[e] /= (double)(N * k);", "f[e] /= (double)N;"),
+    "router_bias_ignored": ("double acc = b_r ? (double)b_r[e] : 0.0;", "double acc = 0.0;"),
+    "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
+}
+
+
+def _run_pins_against(source: str, tmp_path):
+    mut_c = tmp_path / "copy.c"
+    mut_c.write_text(source)
+    so = tmp_path / "libcopy.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                           "-ffp-contract=off", "-o", str(so), str(mut_c), "-lm"])
+    env = dict(os.environ, MOE_ORACLE_LIB=str(so), OMP_NUM_THREADS="2")
+    tests = [os.path.join(ROOT, "tests", f) for f in
+             ("test_oracle_route.py", "test_oracle_permute.py", "test_oracle_layer.py",
+              "test_oracle_stats.py")]
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                           *tests], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+
+
+def test_unmodified_copy_passes(tmp_path):
+    """Control: the same harness on an unmodified copy passes, so a failure below is the
+    planted mistake and not the harness."""
+    r = _run_pins_against(open(SRC).read(), tmp_path)
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    r = _run_pins_against(src.replace(old, new), tmp_path)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout or "error" in r.stdout.lower()
