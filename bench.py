@@ -1,0 +1,358 @@
+"""Benchmark of the MoE layer forward pass on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_forward (router, permute, grouped gate/up and down GEMMs, shared experts,
+combine) over one resident batch of the named workload; the default workload is the
+Mixtral-shaped bf16 layer (N=4096, d=4096, d_ff=14336, E=8, top-2).  Weights (2.8 GB) exceed the
+126 MB L2, so no flush is needed between steps.  `value` is tokens/s over all ranks from CUDA
+events; `e2e` repeats the measurement through the same C ABI with the batch copied in from pinned
+host memory and the output copied back every step.  `roofline` reports the dominant kernel (the
+routed gate/up grouped GEMM) against the measured bf16 peak.  `cpu_baseline` times the CPU oracle
+on a bounded sub-batch of the same layer.  Under torchrun (N > 1) every rank runs its own replica
+(the layer needs no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth  # noqa: E402
+from sparse_conditional_moe_b300 import accounting  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_id_for_smi(torch, local: int) -> str:
+    """nvidia-smi --id of the device torch uses (its UUID, so CUDA_VISIBLE_DEVICES is honoured)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def cpu_oracle_rate(spec, layer_host: dict, budget_s: float, max_steps: int = 0):
+    """Oracle forward over consecutive sub-batches of the layer until budget_s elapses.
+    Returns (tokens/s, tokens processed, seconds, sub-batch size, cores)."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    code = oracle.BF16 if spec.dtype == "bf16" else oracle.F32
+    sub = max(1, min(spec.N, cores))
+    x = layer_host["x"]
+    done, t_used, steps = 0, 0.0, 0
+    start = 0
+    while True:
+        L = dict(layer_host)
+        L["x"] = x[start:start + sub]
+        t0 = time.perf_counter()
+        oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor)
+        t_used += time.perf_counter() - t0
+        done += L["x"].shape[0]
+        steps += 1
+        start = (start + sub) % max(1, spec.N - sub + 1)
+        if t_used >= budget_s or (max_steps and steps >= max_steps):
+            break
+    return done / t_used, done, t_used, sub, cores
+
+
+def host_layer(dev: dict) -> dict:
+    return {k: (None if v is None else v.cpu()) for k, v in dev.items()}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=moe_synth.MIXTRAL.name,
+                    choices=sorted(moe_synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU-oracle budget for the cpu_baseline field (0 to skip)")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = moe_synth.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        return run_reference(args, spec, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from sparse_conditional_moe_b300 import moe
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = moe_synth.make_layer(spec, seed=0, device="cuda")
+    cfg = moe.cfg_from_spec(spec)
+    lay = moe.MoELayer(cfg, dev)
+    xs = [dev["x"], moe_synth.make_x(spec, seed=1000 + rank, device="cuda")]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        lay.forward(xs[i % 2])
+    torch.cuda.synchronize()
+    if lay.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    st = lay.stats()
+    kept_rows, touched = st["kept_rows"], st["touched_experts"]
+
+    # ---------------- device-timed region (inputs resident in HBM)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_TRACE_EVENTS)]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for_smi(torch, local))
+    clocks.start()
+    time.sleep(0.15)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        lay.forward(xs[i % 2], events=ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if lay.device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    ms_step = elapsed_ms / args.steps
+    value = spec.N * world / (ms_step / 1e3)
+
+    phases = ["route", "permute", "gateup", "down", "shared", "combine"]
+    ph_ms = {p: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+             for j, p in enumerate(phases)}
+
+    # ---------------- roofline of the dominant kernel (routed gate/up grouped GEMM)
+    act_b = 2 if spec.dtype == "bf16" else 4
+    gu_flops = accounting.gateup_flops(spec.d, spec.d_ff, kept_rows)
+    gu_s = ph_ms["gateup"] / 1e3
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved_t = gu_flops / gu_s / 1e12
+    work = accounting.layer_work(spec.N, spec.d, spec.d_ff, spec.E, spec.k, spec.n_shared,
+                                 spec.d_ff_shared, act_b, kept_rows, touched)
+    layer_tflops = work.flops / (ms_step / 1e3) / 1e12
+    layer_gbs = work.bytes / (ms_step / 1e3) / 1e9
+    roof_s = work.roofline_s(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+    traffic = read_traffic("gateup")
+
+    # ---------------- end to end through the C ABI with host buffers
+    x_host = [x.cpu().pin_memory() for x in xs]
+    out_host = torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory()
+    x_dev = torch.empty_like(xs[0])
+    e2e_steps = max(3, min(args.steps, 50))
+    for i in range(3):
+        x_dev.copy_(x_host[i % 2], non_blocking=True)
+        out_host.copy_(lay.forward(x_dev), non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        x_dev.copy_(x_host[i % 2], non_blocking=True)
+        out_host.copy_(lay.forward(x_dev), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = spec.N * world / (e2e_ms / 1e3)
+
+    launches_per_step = 2 + 4 + 1 + 2 + (2 if spec.n_shared > 0 else 0) + 1
+
+    # ---------------- CPU oracle on a bounded sub-batch (rank 0 only)
+    cpu = None
+    if rank == 0 and args.cpu_seconds > 0:
+        rate, done, secs, sub, cores = cpu_oracle_rate(spec, host_layer(dev), args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} tokens of {spec.name} in consecutive sub-batches of {sub} "
+                         f"(each its own batch), {secs:.1f} s of CPU work"}
+
+    if rank == 0:
+        line = {
+            "metric": "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
+            if spec is moe_synth.MIXTRAL else f"MoE layer forward tokens/s ({spec.name})",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if act_b == 2 else "f32",
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/d_in) weights)",
+            "config": {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff,
+                       "E": spec.E, "k": spec.k, "n_shared": spec.n_shared,
+                       "capacity_factor": spec.capacity_factor,
+                       "l2": "no flush: weights of %.2f GB exceed the 126 MB L2" %
+                             (3 * spec.E * spec.d * spec.d_ff * act_b / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "layer": {"tflops": layer_tflops, "hbm_gbs_alg": layer_gbs,
+                      "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s * 1e3 / ms_step,
+                      "kept_rows": kept_rows, "touched_experts": touched,
+                      "phase_ms": ph_ms},
+            "roofline": {"kernel": "grouped gate/up SwiGLU GEMM (tcgen05)", "bound": "tensor",
+                         "achieved": achieved_t, "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": achieved_t / peak_t, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a "
+                                        f"continuous loop); burst {peaks['bf16_tflops']}"},
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": spec.N * spec.d * act_b,
+                    "d2h_bytes_per_step": spec.N * spec.d * act_b},
+            "gpu_launches": launches_per_step * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def read_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if its source hash is current."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", "grouped_gemm_tc.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for ln in open(path):
+        parts = [p.strip() for p in ln.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == h:
+            try:
+                return float(parts[2])
+            except ValueError:
+                return None
+    return None
+
+
+def run_reference(args, spec, rank, world):
+    """The CPU oracle timed on this machine's host cores on the same workload and metric."""
+    if rank != 0:
+        return
+    import torch
+    layer = moe_synth.make_layer(spec, seed=0, device="cpu")
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(spec, layer, 0.0, max_steps=1)
+    rates = []
+    t0 = time.perf_counter()
+    total, secs_total = 0, 0.0
+    for _ in range(args.steps):
+        rate, done, secs, sub, cores = cpu_oracle_rate(spec, layer, budget)
+        total += done
+        secs_total += secs
+    wall = time.perf_counter() - t0
+    value = total / secs_total
+    line = {
+        "impl": "reference", "metric": "MoE layer forward tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * spec.N / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff,
+                   "E": spec.E, "k": spec.k},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{total} tokens in sub-batches of {sub}, {secs_total:.1f} s "
+                                   f"of oracle time ({wall:.1f} s wall)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

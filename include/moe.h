@@ -1,0 +1,236 @@
+/*
+ * moe.h -- C ABI of libmoe.so: forward pass of a top-k routed Mixture-of-Experts
+ * SwiGLU FFN layer with optional shared experts, on one B300 GPU (sm_103a).
+ *
+ * The operation is the one defined on the page "混合专家 MoE" (ai-infra-handbooks,
+ * Transformer 解剖), sections "结构" and "实现：逐 token 与按专家分组":
+ *     y_t = sum_{i in TopK(softmax(x_t W_r^T))} w_i(x_t) Expert_i(x_t) + sum_s Shared_s(x_t)
+ *     Expert(x) = W_down (silu(W_gate x) * (W_up x))          (no biases)
+ * with the k weights renormalised to sum to 1, computed in the expert-grouped
+ * organisation of that section (flatten (token, slot), stable sort by expert,
+ * histogram + prefix sum, one grouped GEMM per projection, weighted scatter back).
+ * The capacity limit follows "混合专家模型 (MoE)：大规模稀疏条件计算的架构与工程实践",
+ * section 三.1: each expert takes at most C = ceil(CF * N * k / E) assignments;
+ * an overflowing assignment skips the expert (the token keeps the residual path,
+ * which is the caller's job: out does not include x).
+ *
+ * Conventions for every call
+ *   - Pointers named x, W_*, out, idx, ... are DEVICE pointers owned by the caller;
+ *     pointers named *_host are host pointers.  The library never allocates device
+ *     memory: scratch comes from a caller-provided workspace of moe_workspace_size()
+ *     bytes (256-byte aligned), initialised once with moe_workspace_init().
+ *   - Layouts are row-major with the last index contiguous (nn.Linear weight
+ *     layout: out x in).  Every row start must be 16-byte aligned, i.e. d, d_ff and
+ *     d_ff_shared are multiples of 8 (bf16) or 4 (fp32); base pointers 16-byte aligned.
+ *   - Dtypes: act_dtype MOE_BF16 means x, expert weights, intermediates and out are
+ *     bf16 with fp32 accumulation; MOE_F32 means all of them are fp32.  The router
+ *     weight W_r, its bias b_r, the routing weights w and probabilities are always fp32.
+ *   - stream is a cudaStream_t passed as void*.  Calls enqueue work on it and return
+ *     after host-side validation; only moe_stats and moe_device_error synchronise.
+ *   - Host-detected problems return a moe_status and launch nothing.  Problems found
+ *     on the device (an expert index outside [0,E), a bounded wait that ran out) set
+ *     bits of a sticky error word in the workspace; read it with moe_device_error().
+ *     Kernels never trap.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned pointer, k > E ... */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. bias_mode 2, E > 1024) */
+    MOE_ERR_CUDA = 3,           /* a CUDA runtime call failed */
+    MOE_ERR_DEVICE_BOUNDS = 4,  /* device saw an expert index outside [0, E) */
+    MOE_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out */
+    MOE_ERR_WORKSPACE = 6       /* workspace missing, too small or misaligned */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Layer configuration ("混合专家 MoE", 实现 section: MoE(d, d_ff, n_experts, top_k, n_shared)). */
+typedef struct {
+    int64_t N;                /* tokens in the batch, >= 0 */
+    int32_t d;                /* model dim */
+    int32_t d_ff;             /* routed expert hidden dim F */
+    int32_t E;                /* routed experts, 1..1024 */
+    int32_t k;                /* experts per token, 1..min(E, 16) */
+    int32_t n_shared;         /* shared experts S, 0..8 (always active, weight 1) */
+    int32_t d_ff_shared;      /* shared expert hidden dim F_s (ignored when S = 0) */
+    float capacity_factor;    /* <= 0: no capacity limit; else C = ceil(CF * N * k / E) */
+    int32_t renorm;           /* 1: renormalise the k weights to sum to 1 (the pages' form) */
+    int32_t bias_mode;        /* 0: no router bias; 1: b_r added to the logits before softmax */
+    int32_t act_dtype;        /* moe_dtype */
+} moe_cfg;
+
+/* Device-side error bits of the sticky error word. */
+#define MOE_DEVERR_BOUNDS 1
+#define MOE_DEVERR_TIMEOUT 2
+
+/* Near-tie threshold: a token whose k-th and (k+1)-th router probabilities differ by
+ * less than this is reported by moe_stats (its expert set is not numerically unique). */
+#define MOE_TIE_EPS 1e-6f
+
+/* ------------------------------------------------------------------ workspace */
+
+/* Bytes of device workspace needed by every call below for this cfg. */
+MOE_API moe_status moe_workspace_size(const moe_cfg *cfg, size_t *bytes_host);
+
+/* Clears the sticky device error word.  Call once after allocating the workspace. */
+MOE_API moe_status moe_workspace_init(const moe_cfg *cfg, void *ws, size_t ws_bytes, void *stream);
+
+/* Rows of the expert-grouped buffers: min(N*k, E*C) (N*k without capacity). */
+MOE_API int64_t moe_grouped_rows(const moe_cfg *cfg);
+
+/* ------------------------------------------------------------------ steps */
+
+/*
+ * moe_route -- router ("混合专家 MoE", 实现 section, MoE.route): logits l = x W_r^T (+ b_r),
+ * probabilities p = softmax(l) over all E experts (fp32), the k largest p per token in
+ * descending order (ties to the lower expert index), and w = p_sel / sum(p_sel).
+ *   x [N,d] act dtype; W_r [E,d] fp32; b_r [E] fp32 (used when bias_mode == 1, else ignored)
+ *   idx [N,k] int32 out; w [N,k] fp32 out;
+ *   P_sum [E] fp32 out: sum over tokens of p[t,e] (the load-balance P_e times N);
+ *   gap [N] fp32 out, nullable: p_(k) - p_(k+1) (+inf when k == E).
+ */
+MOE_API moe_status moe_route(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
+                     int32_t *idx, float *w, float *P_sum, float *gap,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_permute -- grouping by expert ("混合专家 MoE", 实现 section, forward_grouped and the
+ * remark after it: counts are a histogram, segment starts a prefix sum) with the capacity
+ * rule of "混合专家模型 (MoE)" section 三.1.  Slot f = t*k + j.
+ *   idx [N,k] int32 in; w [N,k] fp32 in; x [N,d] act dtype in.
+ *   counts [E], offsets [E+1], kept [E], kept_offsets [E+1] int32 out;
+ *   perm [N*k] int32 out: slots stably sorted by expert (bit-identical to a stable sort);
+ *   pos [N*k] int32 out: grouped row of slot f, or -1 when dropped by the capacity;
+ *   row_token [R] int32, row_weight [R] fp32 out: token and routing weight of grouped row r;
+ *   x_perm [R,d] act dtype out: row r = x[row_token[r]].   R = moe_grouped_rows(cfg).
+ * Grouped rows are expert-major; within an expert, kept slots in increasing f.
+ */
+MOE_API moe_status moe_permute(const moe_cfg *cfg, const int32_t *idx, const float *w, const void *x,
+                       int32_t *counts, int32_t *offsets, int32_t *kept, int32_t *kept_offsets,
+                       int32_t *perm, int32_t *pos, int32_t *row_token, float *row_weight,
+                       void *x_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_grouped_ffn -- every routed expert's SwiGLU FFN on its grouped rows as grouped GEMMs
+ * ("混合专家 MoE", 实现 section: after grouping, a single grouped GEMM serves all experts;
+ * Expert.forward):
+ *   h_r = silu(W_gate[e] x_r) * (W_up[e] x_r),   y_r = row_weight[r] * (W_down[e] h_r)
+ * for rows r in [kept_offsets[e], kept_offsets[e] + kept[e]).
+ *   x_perm [R,d]; W_gate, W_up [E,F,d]; W_down [E,d,F] act dtype;
+ *   kept [E], kept_offsets [E+1] int32; row_weight [R] fp32, nullable (weight 1);
+ *   y_perm [R,d] act dtype out.  h is kept in the workspace (bf16 or fp32).
+ */
+MOE_API moe_status moe_grouped_ffn(const moe_cfg *cfg, const void *x_perm, const int32_t *kept,
+                           const int32_t *kept_offsets, const float *row_weight,
+                           const void *W_gate, const void *W_up, const void *W_down,
+                           void *y_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_combine -- weighted scatter back to token order plus the shared experts
+ * ("混合专家 MoE", 结构 section y = sum w_i Expert_i(x); forward_naive/forward_grouped
+ * "+ sum(s(x) for s in shared)"):
+ *   out_t = sum_{j : pos[t*k+j] >= 0} y_perm[pos[t*k+j]] + sum_s Shared_s(x_t)
+ * summed in fp32 in slot order then shared order, rounded once to the act dtype.
+ *   y_perm [R,d] (weights already applied); pos [N*k]; x [N,d];
+ *   Ws_gate, Ws_up [S,F_s,d], Ws_down [S,d,F_s] (NULL when S = 0); out [N,d] out.
+ */
+MOE_API moe_status moe_combine(const moe_cfg *cfg, const void *y_perm, const int32_t *pos, const void *x,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down,
+                       void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ whole layer */
+
+/*
+ * moe_forward -- the whole layer: moe_route, moe_permute, moe_grouped_ffn, moe_combine on
+ * one stream with no host synchronisation; intermediates live in the workspace (see
+ * moe_forward_buffers).  Arguments as in the step calls; out [N,d] act dtype.
+ */
+MOE_API moe_status moe_forward(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       const void *Ws_gate, const void *Ws_up, const void *Ws_down,
+                       void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Phases timed by moe_forward_traced: events[i] is recorded after phase i-1 ends. */
+#define MOE_TRACE_EVENTS 7  /* start, route, permute, gate/up, down, shared, combine */
+
+/*
+ * moe_forward_traced -- moe_forward that also records events[0..6] (cudaEvent_t as void*,
+ * created by the caller) on stream: before routing and after routing, permutation,
+ * routed gate/up GEMM, routed down GEMM, shared experts and combine.
+ */
+MOE_API moe_status moe_forward_traced(const moe_cfg *cfg, const void *x, const float *W_r,
+                              const float *b_r, const void *W_gate, const void *W_up,
+                              const void *W_down, const void *Ws_gate, const void *Ws_up,
+                              const void *Ws_down, void *out, void *ws, size_t ws_bytes,
+                              void *stream, void *const *events);
+
+/* Device pointers of the intermediates moe_forward leaves in the workspace. */
+typedef struct {
+    int32_t *idx;          /* [N,k] */
+    float *w;              /* [N,k] */
+    float *gap;            /* [N] */
+    float *P_sum;          /* [E] */
+    int32_t *counts;       /* [E] */
+    int32_t *offsets;      /* [E+1] */
+    int32_t *kept;         /* [E] */
+    int32_t *kept_offsets; /* [E+1] */
+    int32_t *perm;         /* [N*k] */
+    int32_t *pos;          /* [N*k] */
+    int32_t *row_token;    /* [R] */
+    float *row_weight;     /* [R] */
+    void *x_perm;          /* [R,d] */
+    void *y_perm;          /* [R,d] */
+} moe_buffers;
+
+MOE_API moe_status moe_forward_buffers(const moe_cfg *cfg, void *ws, size_t ws_bytes, moe_buffers *out_host);
+
+/* ------------------------------------------------------------------ statistics */
+
+/* Load-balance statistics ("混合专家 MoE", 负载均衡 section, aux_loss). */
+typedef struct {
+    float aux;                 /* L_aux = E * sum_e f_e P_e */
+    int32_t device_error;      /* the sticky device error word */
+    int64_t dropped;           /* assignments dropped by the capacity */
+    int64_t fully_dropped;     /* tokens with every assignment dropped */
+    int64_t near_tie;          /* tokens with gap < MOE_TIE_EPS */
+    int64_t touched_experts;   /* experts with >= 1 kept row */
+    int64_t kept_rows;         /* sum of kept */
+} moe_stats_summary;
+
+/*
+ * moe_stats -- f_e = counts_e / (N*k) (before dropping), P_e = P_sum_e / N,
+ * L_aux = E * sum_e f_e P_e, and the counters above.  Synchronises the stream.
+ *   counts [E], kept [E], pos [N*k] int32; P_sum [E] fp32; gap [N] fp32 (nullable);
+ *   f_host [E], P_host [E] fp32 host out (nullable); summary_host host out.
+ */
+MOE_API moe_status moe_stats(const moe_cfg *cfg, const int32_t *counts, const int32_t *kept,
+                     const float *P_sum, const int32_t *pos, const float *gap,
+                     float *f_host, float *P_host, moe_stats_summary *summary_host,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises the stream and reads the sticky device error word (MOE_DEVERR_* bits). */
+MOE_API moe_status moe_device_error(void *ws, size_t ws_bytes, int32_t *code_host, void *stream);
+
+MOE_API const char *moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

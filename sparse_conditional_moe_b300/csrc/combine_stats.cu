@@ -1,0 +1,231 @@
+// combine_stats.cu -- weighted combine back to token order, the GEMM tile plan, and the
+// load-balance statistics.
+//
+// Combine (page "混合专家 MoE", section "结构": y = sum_i w_i Expert_i(x), plus the shared
+// expert; forward_grouped scatters the weighted rows back with index_add_): each token
+// gathers its k grouped rows (already multiplied by their routing weight in the down-GEMM
+// epilogue) in slot order, skips dropped slots (pos = -1), adds the shared experts' rows,
+// sums in fp32 and rounds once.  This is a deterministic gather-reduce, not a scatter with
+// atomics.
+//
+// Statistics (same page, section "负载均衡", aux_loss): f_e = counts_e / (N k),
+// P_e = sum_t p[t,e] / N, L_aux = E sum_e f_e P_e, plus dropped / fully-dropped / near-tie
+// counters (integer atomics only, so the result is deterministic).
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void add(const __nv_bfloat16* p, float (&a)[8]) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 f = __bfloat1622float2(h[i]);
+            a[2 * i] += f.x;
+            a[2 * i + 1] += f.y;
+        }
+    }
+    __device__ static void store(__nv_bfloat16* p, const float (&a)[8]) {
+        uint4 v;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = v;
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void add(const float* p, float (&a)[4]) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(p));
+        a[0] += v.x;
+        a[1] += v.y;
+        a[2] += v.z;
+        a[3] += v.w;
+    }
+    __device__ static void store(float* p, const float (&a)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(a[0], a[1], a[2], a[3]);
+    }
+};
+
+// One warp per token, lanes over 16-byte column chunks.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T* __restrict__ ysh,
+               int S, int64_t N, int d, int k, int64_t R, T* __restrict__ out, int32_t* err) {
+    constexpr int V = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int chunks = d / V;
+    for (int64_t t = warp_global; t < N; t += warps) {
+        int32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            p[j] = -1;
+            if (j < k) {
+                int32_t v = pos[t * k + j];
+                if (v >= R) {
+                    if (lane == 0) atomicOr(err, MOE_DEVERR_BOUNDS);
+                    v = -1;
+                }
+                p[j] = v;
+            }
+        }
+        for (int c = lane; c < chunks; c += 32) {
+            float a[V];
+#pragma unroll
+            for (int i = 0; i < V; i++) a[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (j < k && p[j] >= 0) Vec<T>::add(y + (int64_t)p[j] * d + c * V, a);
+            for (int s = 0; s < S; s++) Vec<T>::add(ysh + ((int64_t)s * N + t) * d + c * V, a);
+            Vec<T>::store(out + t * d + c * V, a);
+        }
+    }
+}
+
+// mtile_off[e] = sum_{e' < e} ceil(kept[e'] / bm), one block, E <= 1024.
+__global__ void __launch_bounds__(1024)
+plan_kernel(const int32_t* __restrict__ kept, int E, int bm, int32_t* __restrict__ mtile_off) {
+    __shared__ int tmp[33];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    const int v = e < E ? (kept[e] + bm - 1) / bm : 0;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = tmp[lane];
+        int winc = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, winc, off);
+            if (lane >= off) winc += o;
+        }
+        tmp[lane] = winc - wv;
+        if (lane == 31) tmp[32] = winc;
+    }
+    __syncthreads();
+    if (e < E) mtile_off[e] = tmp[warp] + inc - v;
+    if (e == 0) mtile_off[E] = tmp[32];
+}
+
+// counters[0] fully dropped tokens, [1] near-tie tokens (counters zeroed by the caller)
+__global__ void stats_tokens_kernel(const int32_t* __restrict__ pos, const float* __restrict__ gap,
+                                    int64_t N, int k, int32_t* counters) {
+    int fd = 0, nt = 0;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < N;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        bool any = false;
+        for (int j = 0; j < k; j++) any |= pos[t * k + j] >= 0;
+        fd += !any;
+        if (gap && gap[t] < MOE_TIE_EPS) nt++;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        fd += __shfl_xor_sync(0xffffffffu, fd, off);
+        nt += __shfl_xor_sync(0xffffffffu, nt, off);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (fd) atomicAdd(&counters[0], fd);
+        if (nt) atomicAdd(&counters[1], nt);
+    }
+}
+
+// stats_f layout: f[E], P[E], then aux, dropped (as float bits of int: see host), ...
+__global__ void __launch_bounds__(1024)
+stats_final_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ kept,
+                   const float* __restrict__ P_sum, int64_t N, int E, int k,
+                   float* __restrict__ stats_f, int32_t* counters) {
+    __shared__ float red[32];
+    __shared__ int ired[2][32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    float fp = 0.f;
+    int kp = 0, touched = 0;
+    if (e < E) {
+        const float f = N > 0 ? (float)counts[e] / (float)(N * k) : 0.f;
+        const float P = N > 0 ? P_sum[e] / (float)N : 0.f;
+        stats_f[e] = f;
+        stats_f[E + e] = P;
+        fp = f * P;
+        kp = kept[e];
+        touched = kept[e] > 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        fp += __shfl_xor_sync(0xffffffffu, fp, off);
+        kp += __shfl_xor_sync(0xffffffffu, kp, off);
+        touched += __shfl_xor_sync(0xffffffffu, touched, off);
+    }
+    if (lane == 0) {
+        red[warp] = fp;
+        ired[0][warp] = kp;
+        ired[1][warp] = touched;
+    }
+    __syncthreads();
+    if (e == 0) {
+        float s = 0.f;
+        int ks = 0, ts = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) {
+            s += red[w];
+            ks += ired[0][w];
+            ts += ired[1][w];
+        }
+        stats_f[2 * E] = (float)E * s;
+        counters[2] = ks;   // kept rows
+        counters[3] = ts;   // touched experts
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* pos,
+                           const void* y_sh, void* out, int32_t* err, cudaStream_t s) {
+    if (c.N <= 0) return cudaSuccess;
+    const int64_t R = grouped_rows(c);
+    int64_t want = (c.N + 7) / 8;
+    int blocks = (int)(want < 148 * 16 ? want : 148 * 16);
+    if (c.act_dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            (const __nv_bfloat16*)y_perm, pos, (const __nv_bfloat16*)y_sh, c.n_shared, c.N, c.d,
+            c.k, R, (__nv_bfloat16*)out, err);
+    else
+        combine_kernel<float><<<blocks, 256, 0, s>>>((const float*)y_perm, pos, (const float*)y_sh,
+                                                     c.n_shared, c.N, c.d, c.k, R, (float*)out, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_mtiles(const int32_t* kept, int E, int bm, int32_t* mtile_off,
+                               cudaStream_t s) {
+    plan_kernel<<<1, 1024, 0, s>>>(kept, E, bm, mtile_off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const moe_cfg& c, const int32_t* counts, const int32_t* kept,
+                         const float* P_sum, const int32_t* pos, const float* gap,
+                         int32_t* counters, float* stats_f, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    if (c.N > 0) {
+        int64_t want = (c.N + 255) / 256;
+        int blocks = (int)(want < 148 * 4 ? want : 148 * 4);
+        stats_tokens_kernel<<<blocks, 256, 0, s>>>(pos, gap, c.N, c.k, counters);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    stats_final_kernel<<<1, 1024, 0, s>>>(counts, kept, P_sum, c.N, c.E, c.k, stats_f, counters);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

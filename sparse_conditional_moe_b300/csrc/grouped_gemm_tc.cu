@@ -1,0 +1,588 @@
+// grouped_gemm_tc.cu -- grouped bf16 GEMMs of the expert FFNs on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+//
+// Page "混合专家 MoE", section "实现：逐 token 与按专家分组": after grouping, every expert
+// multiplies all of its tokens at once and a single grouped GEMM serves all experts;
+// Expert.forward is down(silu(gate(x)) * up(x)).  Two kernels:
+//   gate/up : per group g, C[r, n] = silu(A_r . Wg[g,n]) * (A_r . Wu[g,n])   (bf16 out)
+//   down    : per group g, C[r, n] = row_scale[r] * (A_r . Wd[g,n])          (bf16 out)
+// A group owns a contiguous row range of A and C (its kept tokens in grouped order, or all
+// tokens for a shared expert); empty groups own no tile.
+//
+// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128-byte swizzle) per
+//               k-block into a 4-stage shared-memory ring (48 KB per stage);
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
+//               K=16, fp32 accumulate) and frees ring slots with tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the 128x256 fp32 accumulator (each warp its 32-lane
+//               quarter), silu*mul or scale in fp32, one rounding to bf16, 16-byte stores.
+// Two accumulators (2 x 256 columns) let the epilogue of tile i overlap the mainloop of i+1.
+// For gate/up the B tile stacks 128 gate rows over the 128 matching up rows, so one MMA
+// yields both projections of 128 hidden units side by side in TMEM.
+// Tiles are ordered group-major, then n-tile, with the m-tiles of a group innermost, so the
+// CTAs working at the same time share a weight tile through L2.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises an abort flag, the
+// other roles stop at their next wait, in-flight copies and MMAs are drained with bounded
+// waits, TMEM is freed and the device error word gets MOE_DEVERR_TIMEOUT.
+#include <cuda.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, BN = 256, STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;
+constexpr int B_STAGE = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;   // 100 ms
+
+enum { EPI_SWIGLU = 0, EPI_SCALE = 1 };
+
+struct TcParams {
+    int G;
+    const int32_t* rows;
+    const int32_t* row_off;
+    const int32_t* mtile_off;
+    int uniform_rows;
+    int64_t a_stride, c_stride;
+    int K;               // reduction length
+    int n_out;           // valid output columns per group
+    int b_rows;          // rows of B per group in its 2-D map (F for gate/up, d for down)
+    int n_tiles;         // output column tiles per group
+    __nv_bfloat16* C;
+    int64_t ldc;
+    const float* row_scale;
+    int32_t* err;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, cta_group::1.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on an mbarrier once every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
+// 8-row core-matrix groups 1024 bytes apart (stride byte offset), tile base 1024-aligned.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // start address >> 4      [0,14)
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused for SW128 K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset >> 4 [32,46)
+    d |= (uint64_t)1 << 46;                          // descriptor version 0b001 [46,49)
+    d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle [61,64)
+    return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- bounded waits
+
+// One thread.  false when the abort flag is up (if honoured) or the wait timed out.
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                      uint64_t timeout_ns, bool honour_abort) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = gtimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait(a, parity)) return true;
+        if (honour_abort && *abort_flag) return false;
+        if (gtimer() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Whole warp, convergent; every lane returns the same answer.
+__device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        bool ok = mbar_try_wait(a, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if ((it & 63) == 63) {
+            int stop = 0;
+            if (lane == 0) {
+                uint64_t now = gtimer();
+                if (t0 == 0) t0 = now;
+                stop = (*abort_flag != 0) || (now - t0 > kWaitTimeoutNs);
+                if (stop) *abort_flag = 1;
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- tile scheduling
+
+struct TileInfo {
+    int g, mt, nt, rows;
+    int64_t a_row0, c_row0;
+};
+
+__device__ __forceinline__ int total_tiles(const TcParams& p) {
+    if (p.rows == nullptr) return p.G * ((p.uniform_rows + BM - 1) / BM) * p.n_tiles;
+    return p.mtile_off[p.G] * p.n_tiles;
+}
+
+__device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int tile) {
+    TileInfo t;
+    if (p.rows == nullptr) {
+        const int mtg = (p.uniform_rows + BM - 1) / BM;
+        const int per = mtg * p.n_tiles;
+        t.g = tile / per;
+        const int local = tile - t.g * per;
+        t.mt = local % mtg;
+        t.nt = local / mtg;
+        t.rows = p.uniform_rows;
+        t.a_row0 = (int64_t)t.g * p.a_stride;
+        t.c_row0 = (int64_t)t.g * p.c_stride;
+    } else {
+        // largest g with mtile_off[g] * n_tiles <= tile (that group is non-empty)
+        int lo = 0, hi = p.G;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (p.mtile_off[mid] * p.n_tiles <= tile) lo = mid;
+            else hi = mid;
+        }
+        t.g = lo;
+        const int mt0 = p.mtile_off[lo];
+        const int mtg = p.mtile_off[lo + 1] - mt0;
+        const int local = tile - mt0 * p.n_tiles;
+        t.mt = local % mtg;
+        t.nt = local / mtg;
+        t.rows = p.rows[lo];
+        t.a_row0 = t.c_row0 = p.row_off[lo];
+    }
+    return t;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                  const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
+    uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
+    uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
+    uint64_t* tempty = tfull + 2;          // [2]       epilogue -> MMA
+    uint64_t* drain = tempty + 2;          // [1]       MMA drain on exit
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB0);
+        if (EPI == EPI_SWIGLU) prefetch_tmap(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    const int ntiles = total_tiles(p);
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int s = 0;
+            uint32_t ph = 0;
+            int last_ph[STAGES];
+            for (int i = 0; i < STAGES; i++) last_ph[i] = -1;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile(p, tile);
+                const int a_y = (int)(t.a_row0 + (int64_t)t.mt * BM);
+                const int b_y = t.g * p.b_rows + t.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+                for (int kb = 0; kb < nk; kb++) {
+                    if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    const int kx = kb * BK;
+                    tma_load_2d(smem_u32(sA + s * A_STAGE), &tmA, &full[s], kx, a_y);
+                    if (EPI == EPI_SWIGLU) {
+                        tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB0, &full[s], kx, b_y);
+                        tma_load_2d(smem_u32(sB + s * B_STAGE + B_STAGE / 2), &tmB1, &full[s], kx,
+                                    b_y);
+                    } else {
+                        tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB0, &full[s], kx, b_y);
+                    }
+                    last_ph[s] = (int)ph;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA can exit
+                for (int i = 0; i < STAGES; i++)
+                    if (last_ph[i] >= 0)
+                        wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; kb++) {
+                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * A_STAGE);
+                    const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; kk++)
+                        umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&tfull[acc]);
+            }
+            // every MMA issued by this thread completes before TMEM can be released
+            umma_commit(drain);
+            wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..5)
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!waitw(&tfull[acc], aph, abort_flag)) break;
+            tc_fence_after();
+            const TileInfo t = decode_tile(p, tile);
+            const int r = t.mt * BM + row_in_tile;
+            const bool valid = r < t.rows;
+            const int64_t crow = t.c_row0 + r;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (EPI == EPI_SWIGLU) {
+                const int col0 = t.nt * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < (BN / 2) / 32; c++) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(taddr + c * 32, g);
+                    tmem_ld32(taddr + BN / 2 + c * 32, u);
+                    tmem_ld_wait();
+                    if (valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++) {
+                            float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                            float h1 =
+                                silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                            pk[j] = pack_bf16(h0, h1);
+                        }
+                        const int col = col0 + c * 32;
+                        __nv_bfloat16* dst = p.C + crow * p.ldc + col;
+#pragma unroll
+                        for (int v = 0; v < 4; v++)
+                            if (col + v * 8 + 8 <= p.n_out)
+                                *reinterpret_cast<uint4*>(dst + v * 8) =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            } else {
+                const int col0 = t.nt * BN;
+                const float sc = (valid && p.row_scale) ? p.row_scale[crow] : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c++) {
+                    uint32_t a[32];
+                    tmem_ld32(taddr + c * 32, a);
+                    tmem_ld_wait();
+                    if (valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++)
+                            pk[j] = pack_bf16(__uint_as_float(a[2 * j]) * sc,
+                                              __uint_as_float(a[2 * j + 1]) * sc);
+                        const int col = col0 + c * 32;
+                        __nv_bfloat16* dst = p.C + crow * p.ldc + col;
+#pragma unroll
+                        for (int v = 0; v < 4; v++)
+                            if (col + v * 8 + 8 <= p.n_out)
+                                *reinterpret_cast<uint4*>(dst + v * 8) =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && p.err) atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, box = box_rows x 64 columns, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows <= 0 || cols <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TcParams base_params(const GroupGeom& g) {
+    TcParams p{};
+    p.G = g.G;
+    p.rows = g.rows;
+    p.row_off = g.row_off;
+    p.mtile_off = g.mtile_off;
+    p.uniform_rows = g.uniform_rows;
+    p.a_stride = g.a_stride;
+    p.c_stride = g.c_stride;
+    return p;
+}
+
+int grid_for(const GroupGeom& g, int n_tiles) {
+    int64_t max_tiles;
+    if (g.rows == nullptr)
+        max_tiles = (int64_t)g.G * ((g.uniform_rows + BM - 1) / BM) * n_tiles;
+    else
+        max_tiles = ((g.max_rows + BM - 1) / BM + g.G) * (int64_t)n_tiles;
+    int sms = device_sm_count();
+    return (int)(max_tiles < sms ? (max_tiles < 1 ? 1 : max_tiles) : sms);
+}
+
+template <int EPI>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                   const TcParams& p, int grid, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    tc_grouped_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
+                      const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
+                      __nv_bfloat16* H, int64_t h_rows, int32_t* err, cudaStream_t s) {
+    (void)h_rows;
+    if (g.G <= 0 || a_rows <= 0) return cudaSuccess;
+    CUtensorMap ma, mg, mu;
+    if (!make_map(&ma, A, a_rows, K, BM) || !make_map(&mg, Wg, (int64_t)g.G * F, K, BN / 2) ||
+        !make_map(&mu, Wu, (int64_t)g.G * F, K, BN / 2))
+        return cudaErrorInvalidValue;
+    TcParams p = base_params(g);
+    p.K = K;
+    p.n_out = F;
+    p.b_rows = F;
+    p.n_tiles = (F + BN / 2 - 1) / (BN / 2);
+    p.C = H;
+    p.ldc = F;
+    p.row_scale = nullptr;
+    p.err = err;
+    return launch<EPI_SWIGLU>(ma, mg, mu, p, grid_for(g, p.n_tiles), s);
+}
+
+cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
+                    const __nv_bfloat16* Wd, int D, const float* row_scale,
+                    __nv_bfloat16* Y, int64_t y_rows, int32_t* err, cudaStream_t s) {
+    (void)y_rows;
+    if (g.G <= 0 || h_rows <= 0) return cudaSuccess;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, H, h_rows, F, BM) || !make_map(&mb, Wd, (int64_t)g.G * D, F, BN))
+        return cudaErrorInvalidValue;
+    TcParams p = base_params(g);
+    p.K = F;
+    p.n_out = D;
+    p.b_rows = D;
+    p.n_tiles = (D + BN - 1) / BN;
+    p.C = Y;
+    p.ldc = D;
+    p.row_scale = row_scale;
+    p.err = err;
+    return launch<EPI_SCALE>(ma, mb, mb, p, grid_for(g, p.n_tiles), s);
+}
+
+}  // namespace moe

@@ -1,0 +1,456 @@
+// moe_api.cu -- the C ABI of libmoe.so: argument validation, workspace layout and the order of
+// launches for each entry point declared in include/moe.h.
+#include <math.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+int64_t capacity(const moe_cfg& c) {
+    if (!(c.capacity_factor > 0.f)) return -1;
+    return (int64_t)ceil((double)c.capacity_factor * (double)c.N * (double)c.k / (double)c.E);
+}
+
+int64_t grouped_rows(const moe_cfg& c) {
+    const int64_t A = c.N * c.k;
+    const int64_t cap = capacity(c);
+    if (cap < 0) return A;
+    const int64_t lim = cap * c.E;
+    return lim < A ? lim : A;
+}
+
+static size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const moe_cfg& c) {
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += up256(bytes ? bytes : 1);
+        return o;
+    };
+    const int64_t N = c.N, E = c.E, A = c.N * c.k, R = grouped_rows(c);
+    const int64_t S = c.n_shared, F = c.d_ff, Fs = c.d_ff_shared, d = c.d;
+    const size_t esz = c.act_dtype == MOE_BF16 ? 2 : 4;
+    L.err = take(256);
+    L.p_part = take(4 * (size_t)router_blocks(N, (int)E) * E);
+    L.blk_hist = take(4 * (size_t)perm_blocks(A) * E);
+    L.blk_base = take(4 * (size_t)perm_blocks(A) * E);
+    L.mtile_off = take(4 * (size_t)(E + 1));
+    L.stats_f = take(4 * (size_t)(2 * E + 8));
+    L.idx = take(4 * (size_t)A);
+    L.w = take(4 * (size_t)A);
+    L.gap = take(4 * (size_t)N);
+    L.P_sum = take(4 * (size_t)E);
+    L.counts = take(4 * (size_t)E);
+    L.offsets = take(4 * (size_t)(E + 1));
+    L.kept = take(4 * (size_t)E);
+    L.kept_offsets = take(4 * (size_t)(E + 1));
+    L.perm = take(4 * (size_t)A);
+    L.pos = take(4 * (size_t)A);
+    L.row_token = take(4 * (size_t)R);
+    L.row_weight = take(4 * (size_t)R);
+    L.x_perm = take(esz * (size_t)R * d);
+    L.h_perm = take(esz * (size_t)R * F);
+    L.y_perm = take(esz * (size_t)R * d);
+    L.h_sh = take(esz * (size_t)(S * N) * Fs);
+    L.y_sh = take(esz * (size_t)(S * N) * d);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_cfg(const moe_cfg* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->N < 0 || c->d <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0 || c->n_shared < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+    if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
+    if (c->bias_mode < 0 || c->bias_mode > 2) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared > 0 && c->d_ff_shared <= 0) return MOE_ERR_INVALID_ARG;
+    const int mult = c->act_dtype == MOE_BF16 ? 8 : 4;   // 16-byte rows
+    if (c->d % mult || c->d_ff % mult || (c->n_shared > 0 && c->d_ff_shared % mult))
+        return MOE_ERR_INVALID_ARG;
+    if (isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if (c->E > 1024 || c->k > 16 || c->n_shared > 8) return MOE_ERR_UNSUPPORTED;
+    if (c->bias_mode == 2) return MOE_ERR_UNSUPPORTED;
+    if (c->N * (int64_t)c->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if (grouped_rows(*c) * (int64_t)(c->d > c->d_ff ? c->d : c->d_ff) >= ((int64_t)1 << 40))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_cfg* c, void* ws, size_t ws_bytes) {
+    if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*c).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                         \
+    do {                                      \
+        moe_status _s = (expr);               \
+        if (_s != MOE_OK) return _s;          \
+    } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+moe_status need(const void* p, size_t align) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    return aligned(p, align) ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+// --------------------------------------------------------------------- shared pieces
+
+moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* kept,
+                          const int32_t* kept_offsets, const float* row_weight, const void* Wg,
+                          const void* Wu, const void* Wd, void* y_perm, void* ws,
+                          cudaStream_t s, void* const* ev) {
+    const WsLayout L = ws_layout(*c);
+    int32_t* err = at<int32_t>(ws, L.err);
+    int32_t* mtile = at<int32_t>(ws, L.mtile_off);
+    const int64_t R = grouped_rows(*c);
+    const bool bf16 = c->act_dtype == MOE_BF16;
+    MOE_CUDA(launch_plan_mtiles(kept, c->E, bf16 ? kTcBlockRows : simt_block_rows(), mtile, s));
+    GroupGeom g{};
+    g.G = c->E;
+    g.rows = kept;
+    g.row_off = kept_offsets;
+    g.mtile_off = mtile;
+    g.max_rows = R;
+    void* h = at<void>(ws, L.h_perm);
+    if (bf16) {
+        MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
+                           (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
+    } else {
+        MOE_CUDA(simt_gateup_f32(g, (const float*)x_perm, c->d, (const float*)Wg,
+                                 (const float*)Wu, c->d_ff, (float*)h, s));
+    }
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
+    if (bf16) {
+        MOE_CUDA(tc_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
+                         row_weight, (__nv_bfloat16*)y_perm, R, err, s));
+    } else {
+        MOE_CUDA(simt_down_f32(g, (const float*)h, c->d_ff, (const float*)Wd, c->d, row_weight,
+                               (float*)y_perm, s));
+    }
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
+    return MOE_OK;
+}
+
+moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
+                                 const void* x, const void* Wsg, const void* Wsu, const void* Wsd,
+                                 void* out, void* ws, cudaStream_t s, void* const* ev) {
+    const WsLayout L = ws_layout(*c);
+    int32_t* err = at<int32_t>(ws, L.err);
+    void* hsh = at<void>(ws, L.h_sh);
+    void* ysh = at<void>(ws, L.y_sh);
+    const int S = c->n_shared, Fs = c->d_ff_shared;
+    if (S > 0 && c->N > 0) {
+        GroupGeom g{};
+        g.G = S;
+        g.uniform_rows = (int)c->N;
+        g.max_rows = c->N;
+        if (c->act_dtype == MOE_BF16) {
+            g.a_stride = 0;        // every shared expert reads all tokens of x
+            g.c_stride = c->N;
+            MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x, c->N, c->d, (const __nv_bfloat16*)Wsg,
+                               (const __nv_bfloat16*)Wsu, Fs, (__nv_bfloat16*)hsh, S * c->N, err, s));
+            g.a_stride = c->N;
+            MOE_CUDA(tc_down(g, (const __nv_bfloat16*)hsh, S * c->N, Fs, (const __nv_bfloat16*)Wsd,
+                             c->d, nullptr, (__nv_bfloat16*)ysh, S * c->N, err, s));
+        } else {
+            g.a_stride = 0;
+            g.c_stride = c->N;
+            MOE_CUDA(simt_gateup_f32(g, (const float*)x, c->d, (const float*)Wsg, (const float*)Wsu,
+                                     Fs, (float*)hsh, s));
+            g.a_stride = c->N;
+            MOE_CUDA(simt_down_f32(g, (const float*)hsh, Fs, (const float*)Wsd, c->d, nullptr,
+                                   (float*)ysh, s));
+        }
+    }
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
+    MOE_CUDA(launch_combine(*c, y_perm, pos, ysh, out, err, s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
+    return MOE_OK;
+}
+
+moe_status check_weights(const moe_cfg* c, const void* Wg, const void* Wu, const void* Wd) {
+    MOE_TRY(need(Wg, 16));
+    MOE_TRY(need(Wu, 16));
+    MOE_TRY(need(Wd, 16));
+    return MOE_OK;
+    (void)c;
+}
+
+moe_status check_shared(const moe_cfg* c, const void* a, const void* b, const void* d) {
+    if (c->n_shared == 0) return MOE_OK;
+    MOE_TRY(need(a, 16));
+    MOE_TRY(need(b, 16));
+    MOE_TRY(need(d, 16));
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_BOUNDS: return "device saw an out-of-range index";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    }
+    return "unknown status";
+}
+
+int64_t moe_grouped_rows(const moe_cfg* cfg) {
+    if (check_cfg(cfg) != MOE_OK) return -1;
+    return grouped_rows(*cfg);
+}
+
+moe_status moe_workspace_size(const moe_cfg* cfg, size_t* bytes) {
+    MOE_TRY(check_cfg(cfg));
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
+                     int32_t* idx, float* w, float* P_sum, float* gap, void* ws, size_t ws_bytes,
+                     void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (cfg->N > 0) {
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(idx, 4));
+        MOE_TRY(need(w, 4));
+    }
+    MOE_TRY(need(W_r, 16));
+    MOE_TRY(need(P_sum, 4));
+    if (cfg->bias_mode == 1) MOE_TRY(need(b_r, 4));
+    const WsLayout L = ws_layout(*cfg);
+    MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.p_part), P_sum,
+                           (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_permute(const moe_cfg* cfg, const int32_t* idx, const float* w, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_offsets,
+                       int32_t* perm, int32_t* pos, int32_t* row_token, float* row_weight,
+                       void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(counts, 4));
+    MOE_TRY(need(offsets, 4));
+    MOE_TRY(need(kept, 4));
+    MOE_TRY(need(kept_offsets, 4));
+    if (cfg->N > 0) {
+        MOE_TRY(need(idx, 4));
+        MOE_TRY(need(w, 4));
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(perm, 4));
+        MOE_TRY(need(pos, 4));
+        MOE_TRY(need(row_token, 4));
+        MOE_TRY(need(row_weight, 4));
+        MOE_TRY(need(x_perm, 16));
+    }
+    const WsLayout L = ws_layout(*cfg);
+    MOE_CUDA(launch_permute(*cfg, idx, w, x, counts, offsets, kept, kept_offsets, perm, pos,
+                            row_token, row_weight, x_perm, at<int32_t>(ws, L.blk_hist),
+                            at<int32_t>(ws, L.blk_base), at<int32_t>(ws, L.err),
+                            (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_grouped_ffn(const moe_cfg* cfg, const void* x_perm, const int32_t* kept,
+                           const int32_t* kept_offsets, const float* row_weight,
+                           const void* W_gate, const void* W_up, const void* W_down, void* y_perm,
+                           void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(kept, 4));
+    MOE_TRY(need(kept_offsets, 4));
+    MOE_TRY(check_weights(cfg, W_gate, W_up, W_down));
+    if (grouped_rows(*cfg) > 0) {
+        MOE_TRY(need(x_perm, 16));
+        MOE_TRY(need(y_perm, 16));
+        if (row_weight) MOE_TRY(need(row_weight, 4));
+    }
+    return do_grouped_ffn(cfg, x_perm, kept, kept_offsets, row_weight, W_gate, W_up, W_down,
+                          y_perm, ws, (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_combine(const moe_cfg* cfg, const void* y_perm, const int32_t* pos, const void* x,
+                       const void* Ws_gate, const void* Ws_up, const void* Ws_down, void* out,
+                       void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(check_shared(cfg, Ws_gate, Ws_up, Ws_down));
+    if (cfg->N > 0) {
+        MOE_TRY(need(pos, 4));
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(out, 16));
+        if (grouped_rows(*cfg) > 0) MOE_TRY(need(y_perm, 16));
+    }
+    return do_shared_and_combine(cfg, y_perm, pos, x, Ws_gate, Ws_up, Ws_down, out, ws,
+                                 (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_r,
+                              const float* b_r, const void* W_gate, const void* W_up,
+                              const void* W_down, const void* Ws_gate, const void* Ws_up,
+                              const void* Ws_down, void* out, void* ws, size_t ws_bytes,
+                              void* stream, void* const* ev) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(W_r, 16));
+    if (cfg->bias_mode == 1) MOE_TRY(need(b_r, 4));
+    MOE_TRY(check_weights(cfg, W_gate, W_up, W_down));
+    MOE_TRY(check_shared(cfg, Ws_gate, Ws_up, Ws_down));
+    if (cfg->N > 0) {
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(out, 16));
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(*cfg);
+    int32_t* err = at<int32_t>(ws, L.err);
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
+                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum), s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
+    MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
+                            at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                            at<int32_t>(ws, L.kept), at<int32_t>(ws, L.kept_offsets),
+                            at<int32_t>(ws, L.perm), at<int32_t>(ws, L.pos),
+                            at<int32_t>(ws, L.row_token), at<float>(ws, L.row_weight),
+                            at<void>(ws, L.x_perm), at<int32_t>(ws, L.blk_hist),
+                            at<int32_t>(ws, L.blk_base), err, s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
+    MOE_TRY(do_grouped_ffn(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
+                           at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), W_gate,
+                           W_up, W_down, at<void>(ws, L.y_perm), ws, s, ev));
+    MOE_TRY(do_shared_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, Ws_gate,
+                                  Ws_up, Ws_down, out, ws, s, ev));
+    return MOE_OK;
+}
+
+moe_status moe_forward(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
+                       const void* W_gate, const void* W_up, const void* W_down,
+                       const void* Ws_gate, const void* Ws_up, const void* Ws_down, void* out,
+                       void* ws, size_t ws_bytes, void* stream) {
+    return moe_forward_traced(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, out,
+                              ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_buffers(const moe_cfg* cfg, void* ws, size_t ws_bytes, moe_buffers* out) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (!out) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*cfg);
+    out->idx = at<int32_t>(ws, L.idx);
+    out->w = at<float>(ws, L.w);
+    out->gap = at<float>(ws, L.gap);
+    out->P_sum = at<float>(ws, L.P_sum);
+    out->counts = at<int32_t>(ws, L.counts);
+    out->offsets = at<int32_t>(ws, L.offsets);
+    out->kept = at<int32_t>(ws, L.kept);
+    out->kept_offsets = at<int32_t>(ws, L.kept_offsets);
+    out->perm = at<int32_t>(ws, L.perm);
+    out->pos = at<int32_t>(ws, L.pos);
+    out->row_token = at<int32_t>(ws, L.row_token);
+    out->row_weight = at<float>(ws, L.row_weight);
+    out->x_perm = at<void>(ws, L.x_perm);
+    out->y_perm = at<void>(ws, L.y_perm);
+    return MOE_OK;
+}
+
+moe_status moe_stats(const moe_cfg* cfg, const int32_t* counts, const int32_t* kept,
+                     const float* P_sum, const int32_t* pos, const float* gap, float* f_host,
+                     float* P_host, moe_stats_summary* summary, void* ws, size_t ws_bytes,
+                     void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(counts, 4));
+    MOE_TRY(need(kept, 4));
+    MOE_TRY(need(P_sum, 4));
+    if (cfg->N > 0) MOE_TRY(need(pos, 4));
+    if (!summary) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(*cfg);
+    int32_t* errw = at<int32_t>(ws, L.err);
+    int32_t* counters = errw + 8;
+    float* sf = at<float>(ws, L.stats_f);
+    MOE_CUDA(launch_stats(*cfg, counts, kept, P_sum, pos, gap, counters, sf, s));
+    const int E = cfg->E;
+    int32_t hc[9];
+    float hscal = 0.f;
+    MOE_CUDA(cudaMemcpyAsync(hc, errw, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaMemcpyAsync(hc + 1, counters, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaMemcpyAsync(&hscal, sf + 2 * E, sizeof(float), cudaMemcpyDeviceToHost, s));
+    if (f_host) MOE_CUDA(cudaMemcpyAsync(f_host, sf, E * sizeof(float), cudaMemcpyDeviceToHost, s));
+    if (P_host)
+        MOE_CUDA(cudaMemcpyAsync(P_host, sf + E, E * sizeof(float), cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaStreamSynchronize(s));
+    summary->aux = hscal;
+    summary->device_error = hc[0];
+    summary->fully_dropped = hc[1];
+    summary->near_tie = hc[2];
+    summary->kept_rows = hc[3];
+    summary->touched_experts = hc[4];
+    summary->dropped = cfg->N * cfg->k - (int64_t)hc[3];
+    return MOE_OK;
+}
+
+moe_status moe_device_error(void* ws, size_t ws_bytes, int32_t* code, void* stream) {
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+    if (!code) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA(cudaMemcpyAsync(code, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    MOE_CUDA(cudaStreamSynchronize(s));
+    if (*code & MOE_DEVERR_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+    if (*code & MOE_DEVERR_BOUNDS) return MOE_ERR_DEVICE_BOUNDS;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// moe_internal.cuh -- device-side declarations shared by the libmoe CUDA sources.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ router tiling
+
+// Tokens per router block for a padded expert count (see router.cu).
+int router_block_tokens(int E);
+int router_blocks(int64_t N, int E);
+
+// ------------------------------------------------------------------ permute tiling
+
+constexpr int kPermThreads = 256;                    // 8 warps
+constexpr int kPermSlotsPerWarp = 256;               // 8 steps of 32 slots
+constexpr int kPermSlotsPerBlock = kPermSlotsPerWarp * (kPermThreads / 32);
+inline int perm_blocks(int64_t slots) {
+    return (int)((slots + kPermSlotsPerBlock - 1) / kPermSlotsPerBlock);
+}
+
+// ------------------------------------------------------------------ workspace
+
+struct WsLayout {
+    size_t err;          // int32 [64]: [0] sticky error word, [8..15] stats counters
+    size_t p_part;       // float [router_blocks * E]
+    size_t blk_hist;     // int32 [perm_blocks * E]
+    size_t blk_base;     // int32 [perm_blocks * E]
+    size_t mtile_off;    // int32 [E + 1]: m-tile prefix of the routed grouped GEMMs
+    size_t stats_f;      // float [2E + 8]: f, P, scalars
+    size_t idx, w, gap, P_sum, counts, offsets, kept, kept_offsets, perm, pos;
+    size_t row_token, row_weight;
+    size_t x_perm, h_perm, y_perm;   // [R, d], [R, F], [R, d]
+    size_t h_sh, y_sh;               // [S, N, F_s], [S, N, d]
+    size_t total;
+};
+
+int64_t grouped_rows(const moe_cfg& c);
+int64_t capacity(const moe_cfg& c);  // -1 when unlimited
+WsLayout ws_layout(const moe_cfg& c);
+
+// ------------------------------------------------------------------ launches
+// All return cudaGetLastError() of their launches.
+
+cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
+                          int32_t* idx, float* w, float* gap, float* p_part, float* P_sum,
+                          cudaStream_t s);
+
+cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w, const void* x,
+                           int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_off,
+                           int32_t* perm, int32_t* pos, int32_t* row_token, float* row_weight,
+                           void* x_perm, int32_t* blk_hist, int32_t* blk_base, int32_t* err,
+                           cudaStream_t s);
+
+// Grouped GEMM problem: G groups; group g owns rows [row0_g, row0_g + rows_g) of A and C.
+struct GroupGeom {
+    int G;
+    const int32_t* rows;       // [G] device, or nullptr for uniform rows
+    const int32_t* row_off;    // [G] device (A and C row offsets), or nullptr for uniform
+    const int32_t* mtile_off;  // [G+1] device m-tile prefix (non-uniform)
+    int uniform_rows;          // rows per group when rows == nullptr
+    int64_t a_stride;          // uniform: A row offset of group g = g * a_stride
+    int64_t c_stride;          // uniform: C row offset of group g = g * c_stride
+    int64_t max_rows;          // upper bound of total rows (grid sizing / tensor extents)
+};
+
+// m-tile prefix over groups for the routed experts (from kept); bm = the GEMM's tile height.
+constexpr int kTcBlockRows = 128;
+cudaError_t launch_plan_mtiles(const int32_t* kept, int E, int bm, int32_t* mtile_off,
+                               cudaStream_t s);
+
+// bf16 tcgen05 grouped SwiGLU (gate|up) GEMM: H = silu(A Wg^T) * (A Wu^T)
+cudaError_t tc_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
+                      const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
+                      __nv_bfloat16* H, int64_t h_rows, int32_t* err, cudaStream_t s);
+// bf16 tcgen05 grouped down GEMM: Y = row_scale * (H Wd^T)
+cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
+                    const __nv_bfloat16* Wd, int D, const float* row_scale,
+                    __nv_bfloat16* Y, int64_t y_rows, int32_t* err, cudaStream_t s);
+
+// fp32 CUDA-core grouped GEMMs (fp32 layers); their m-tiles are simt_block_rows() tall
+int simt_block_rows();
+cudaError_t simt_gateup_f32(const GroupGeom& g, const float* A, int K, const float* Wg,
+                            const float* Wu, int F, float* H, cudaStream_t s);
+cudaError_t simt_down_f32(const GroupGeom& g, const float* H, int F, const float* Wd, int D,
+                          const float* row_scale, float* Y, cudaStream_t s);
+
+cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* pos,
+                           const void* y_sh, void* out, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_stats(const moe_cfg& c, const int32_t* counts, const int32_t* kept,
+                         const float* P_sum, const int32_t* pos, const float* gap,
+                         int32_t* counters, float* stats_f, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

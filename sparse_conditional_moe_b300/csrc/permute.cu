@@ -1,0 +1,245 @@
+// permute.cu -- grouping of (token, slot) assignments by expert, with the capacity limit.
+//
+// Page "混合专家 MoE", section "实现：逐 token 与按专家分组": forward_grouped flattens the
+// (token, slot) pairs (slot f = t*k + j), stably sorts them by expert, counts per expert
+// (bincount) and walks the segments from their running start; the remark after the listing
+// names the pieces: the counts are a histogram and the segment starts a prefix sum.  The
+// capacity rule is from "混合专家模型 (MoE)", section 三.1: an expert keeps at most C
+// assignments; the first C in the stable order are kept, the rest skip the experts.
+//
+// The stable sort is rebuilt from integer counting, so it is bit-identical to a stable
+// argsort and does not depend on thread timing:
+//   count   : block b counts its 2048 consecutive slots per expert (per-warp rows in
+//             shared memory, warp-aggregated with __match_any_sync) -> blk_hist[b][e]
+//   scan    : one block turns blk_hist into counts, offsets (exclusive scan over e),
+//             kept = min(counts, C), kept_offsets, and blk_base[b][e] = offsets-free
+//             prefix of blk_hist over blocks b' < b
+//   scatter : block b recounts per warp, scans over warps, then each warp walks its slots in
+//             order; rank r = blk_base + earlier warps + earlier lanes (__popc of the match
+//             mask below the lane) + earlier steps.  perm[offsets[e] + r] = f,
+//             pos[f] = kept_offsets[e] + r if r < kept[e] else -1
+//   gather  : row r of x_perm = x[row_token[r]], 16-byte vector copies, warp per row.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = kPermThreads / 32;
+
+__device__ __forceinline__ void set_err(int32_t* err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// Per-warp expert counts of this block's slots into cnt[warp][e] (E entries per warp).
+__device__ __forceinline__ void warp_count(const int32_t* __restrict__ idx, int64_t A, int E,
+                                           int64_t f_begin, int* cnt_row, int32_t* err) {
+    const int lane = threadIdx.x & 31;
+    for (int step = 0; step < kPermSlotsPerWarp / 32; step++) {
+        int64_t f = f_begin + step * 32 + lane;
+        int e = -1;
+        if (f < A) {
+            e = idx[f];
+            if (e < 0 || e >= E) {
+                set_err(err, MOE_DEVERR_BOUNDS);
+                e = -1;
+            }
+        }
+        unsigned mask = __match_any_sync(0xffffffffu, e);
+        int leader = __ffs(mask) - 1;
+        if (e >= 0 && lane == leader) cnt_row[e] += __popc(mask);
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_count_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __restrict__ blk_hist,
+                  int32_t* err) {
+    extern __shared__ int cnt[];   // [kWarps][E]
+    const int warp = threadIdx.x / 32;
+    for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    int64_t f0 = (int64_t)blockIdx.x * kPermSlotsPerBlock + (int64_t)warp * kPermSlotsPerWarp;
+    warp_count(idx, A, E, f0, cnt + warp * E, err);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        int s = 0;
+        for (int w = 0; w < kWarps; w++) s += cnt[w * E + e];
+        blk_hist[(int64_t)blockIdx.x * E + e] = s;
+    }
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block (deterministic).
+__device__ int block_exclusive_scan(int v, int* tmp /*[32]*/, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = lane < (int)(blockDim.x >> 5) ? tmp[lane] : 0;
+        int winc = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, winc, off);
+            if (lane >= off) winc += o;
+        }
+        tmp[lane] = winc - wv;   // exclusive prefix of warp totals
+        if (lane == 31) tmp[32] = winc;
+    }
+    __syncthreads();
+    int res = tmp[warp] + inc - v;
+    *total = tmp[32];
+    __syncthreads();
+    return res;
+}
+
+__global__ void __launch_bounds__(1024)
+perm_scan_kernel(const int32_t* __restrict__ blk_hist, int blocks, int E, int64_t cap,
+                 int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ kept,
+                 int32_t* __restrict__ kept_off) {
+    __shared__ int tmp[33];
+    const int e = threadIdx.x;
+    int c = 0;
+    if (e < E) {
+        for (int b = 0; b < blocks; b++) {
+            int h = blk_hist[(int64_t)b * E + e];
+            blk_base[(int64_t)b * E + e] = c;
+            c += h;
+        }
+    }
+    int kp = (cap >= 0 && c > cap) ? (int)cap : c;
+    int total;
+    int off = block_exclusive_scan(e < E ? c : 0, tmp, &total);
+    int koff_total;
+    int koff = block_exclusive_scan(e < E ? kp : 0, tmp, &koff_total);
+    if (e < E) {
+        counts[e] = c;
+        offsets[e] = off;
+        kept[e] = kp;
+        kept_off[e] = koff;
+    }
+    if (e == 0) {
+        offsets[E] = total;
+        kept_off[E] = koff_total;
+    }
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int k,
+                    int E, const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+                    const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_off,
+                    int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+                    int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
+    extern __shared__ int cnt[];   // [kWarps][E] counts, then running bases
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    const int64_t f0 = (int64_t)blockIdx.x * kPermSlotsPerBlock + (int64_t)warp * kPermSlotsPerWarp;
+    warp_count(idx, A, E, f0, cnt + warp * E, nullptr);
+    __syncthreads();
+    // per expert: exclusive scan over warps, starting at this block's base
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        int run = blk_base[(int64_t)blockIdx.x * E + e];
+        for (int wv = 0; wv < kWarps; wv++) {
+            int c = cnt[wv * E + e];
+            cnt[wv * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    int* base = cnt + warp * E;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int step = 0; step < kPermSlotsPerWarp / 32; step++) {
+        int64_t f = f0 + step * 32 + lane;
+        int e = -1;
+        if (f < A) {
+            e = idx[f];
+            if (e < 0 || e >= E) e = -1;
+        }
+        unsigned mask = __match_any_sync(0xffffffffu, e);
+        int r = 0;
+        if (e >= 0) r = base[e] + __popc(mask & lt);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(mask) - 1) base[e] += __popc(mask);
+        __syncwarp();
+        if (f < A) {
+            if (e >= 0) {
+                perm[offsets[e] + r] = (int32_t)f;
+                if (r < kept[e]) {
+                    int p = kept_off[e] + r;
+                    pos[f] = p;
+                    row_token[p] = (int32_t)(f / k);
+                    row_weight[p] = w ? w[f] : 1.f;
+                } else {
+                    pos[f] = -1;
+                }
+            } else {
+                pos[f] = -1;
+            }
+        }
+    }
+}
+
+// x_perm[r] = x[row_token[r]] for r < kept_off[E]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_token,
+                   const int32_t* __restrict__ kept_off_end, int64_t N, int row_vecs,
+                   uint4* __restrict__ xp, int32_t* err) {
+    const int64_t rows = *kept_off_end;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp_global; r < rows; r += warps) {
+        int64_t t = row_token[r];
+        if (t < 0 || t >= N) {
+            if (lane == 0) set_err(err, MOE_DEVERR_BOUNDS);
+            continue;
+        }
+        const uint4* src = x + t * row_vecs;
+        uint4* dst = xp + r * row_vecs;
+        for (int v = lane; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w, const void* x,
+                           int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_off,
+                           int32_t* perm, int32_t* pos, int32_t* row_token, float* row_weight,
+                           void* x_perm, int32_t* blk_hist, int32_t* blk_base, int32_t* err,
+                           cudaStream_t s) {
+    const int64_t A = c.N * c.k;
+    const int E = c.E;
+    const int blocks = perm_blocks(A);
+    const size_t smem = sizeof(int) * kWarps * E;
+    if (blocks > 0) {
+        perm_count_kernel<<<blocks, kPermThreads, smem, s>>>(idx, A, E, blk_hist, err);
+        cudaError_t e1 = cudaGetLastError();
+        if (e1 != cudaSuccess) return e1;
+    }
+    perm_scan_kernel<<<1, 1024, 0, s>>>(blk_hist, blocks, E, capacity(c), blk_base, counts,
+                                        offsets, kept, kept_off);
+    cudaError_t e2 = cudaGetLastError();
+    if (e2 != cudaSuccess || blocks == 0) return e2;
+    perm_scatter_kernel<<<blocks, kPermThreads, smem, s>>>(idx, w, A, c.k, E, blk_base, offsets,
+                                                           kept, kept_off, perm, pos, row_token,
+                                                           row_weight);
+    cudaError_t e3 = cudaGetLastError();
+    if (e3 != cudaSuccess || x_perm == nullptr) return e3;
+    const int esz = c.act_dtype == MOE_BF16 ? 2 : 4;
+    const int row_vecs = (int)((int64_t)c.d * esz / 16);
+    const int64_t rows = grouped_rows(c);
+    int64_t want = (rows + 7) / 8;     // 8 warps per block
+    int gblocks = (int)(want < 148 * 16 ? want : 148 * 16);
+    if (gblocks < 1) gblocks = 1;
+    gather_rows_kernel<<<gblocks, 256, 0, s>>>((const uint4*)x, row_token, kept_off + E, c.N,
+                                               row_vecs, (uint4*)x_perm, err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

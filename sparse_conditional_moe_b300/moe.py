@@ -1,0 +1,282 @@
+"""ctypes binding of libmoe.so: the same entry points as include/moe.h, taking torch tensors.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+There is no fallback: if libmoe.so is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_DEVERR_BOUNDS, MOE_DEVERR_TIMEOUT = 1, 2
+MOE_TRACE_EVENTS = 7
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_DEVICE_BOUNDS", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_WORKSPACE"}
+
+# Every function the header declares (checked against the library's exports by the tests).
+EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_route",
+           "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_forward", "moe_forward_traced",
+           "moe_forward_buffers", "moe_stats", "moe_device_error", "moe_status_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class MoeCfg(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+                ("d_ff_shared", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("renorm", ctypes.c_int32), ("bias_mode", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32)]
+
+
+class MoeBuffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("idx", "w", "gap", "P_sum", "counts", "offsets", "kept", "kept_offsets", "perm",
+                 "pos", "row_token", "row_weight", "x_perm", "y_perm")]
+
+
+class MoeStatsSummary(ctypes.Structure):
+    _fields_ = [("aux", ctypes.c_float), ("device_error", ctypes.c_int32),
+                ("dropped", ctypes.c_int64), ("fully_dropped", ctypes.c_int64),
+                ("near_tie", ctypes.c_int64), ("touched_experts", ctypes.c_int64),
+                ("kept_rows", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m sparse_conditional_moe_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        C = ctypes.POINTER(MoeCfg)
+        sig = {
+            "moe_workspace_size": [C, ctypes.POINTER(SZ)],
+            "moe_workspace_init": [C, P, SZ, P],
+            "moe_route": [C, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_permute": [C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_grouped_ffn": [C, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_combine": [C, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_forward": [C, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_forward_traced": [C, P, P, P, P, P, P, P, P, P, P, P, SZ, P, P],
+            "moe_forward_buffers": [C, P, SZ, ctypes.POINTER(MoeBuffers)],
+            "moe_stats": [C, P, P, P, P, P, P, P, ctypes.POINTER(MoeStatsSummary), P, SZ, P],
+            "moe_device_error": [P, SZ, ctypes.POINTER(ctypes.c_int32), P],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.moe_grouped_rows.argtypes = [C]
+        L.moe_grouped_rows.restype = I64
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_cfg(N: int, d: int, d_ff: int, E: int, k: int, n_shared: int = 0, d_ff_shared: int = 0,
+             capacity_factor: float = 0.0, renorm: int = 1, bias_mode: int = 0,
+             act_dtype: int = MOE_BF16) -> MoeCfg:
+    return MoeCfg(N, d, d_ff, E, k, n_shared, d_ff_shared if n_shared else 0, capacity_factor,
+                  renorm, bias_mode, act_dtype)
+
+
+def cfg_from_spec(spec, N: Optional[int] = None) -> MoeCfg:
+    """MoeCfg of a moe_synth.LayerSpec (bias_mode 1 when the layer has a router bias)."""
+    return make_cfg(spec.N if N is None else N, spec.d, spec.d_ff, spec.E, spec.k, spec.n_shared,
+                    spec.d_ff_shared, spec.capacity_factor, spec.renorm,
+                    1 if getattr(spec, "zipf_bias", 0) > 0 else 0,
+                    MOE_BF16 if spec.dtype == "bf16" else MOE_F32)
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ workspace
+
+def moe_workspace_size(cfg: MoeCfg) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_grouped_rows(cfg: MoeCfg) -> int:
+    r = lib().moe_grouped_rows(ctypes.byref(cfg))
+    if r < 0:
+        raise MoeError(1, "moe_grouped_rows")
+    return r
+
+
+def moe_workspace_init(cfg: MoeCfg, ws: torch.Tensor, stream=None):
+    _check(lib().moe_workspace_init(ctypes.byref(cfg), _p(ws), ws.numel(), _s(stream)),
+           "moe_workspace_init")
+
+
+def workspace(cfg: MoeCfg, device="cuda", stream=None) -> torch.Tensor:
+    """Allocate (torch) and initialise a workspace of moe_workspace_size bytes."""
+    ws = torch.empty(moe_workspace_size(cfg), dtype=torch.uint8, device=device)
+    if ws.data_ptr() % 256:
+        raise RuntimeError("torch returned a workspace that is not 256-byte aligned")
+    moe_workspace_init(cfg, ws, stream)
+    return ws
+
+
+# ------------------------------------------------------------------ steps
+
+def moe_route(cfg, x, W_r, b_r, idx, w, P_sum, gap, ws, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(idx), _p(w), _p(P_sum),
+                           _p(gap), _p(ws), ws.numel(), _s(stream)), "moe_route")
+
+
+def moe_permute(cfg, idx, w, x, counts, offsets, kept, kept_offsets, perm, pos, row_token,
+                row_weight, x_perm, ws, stream=None):
+    _check(lib().moe_permute(ctypes.byref(cfg), _p(idx), _p(w), _p(x), _p(counts), _p(offsets),
+                             _p(kept), _p(kept_offsets), _p(perm), _p(pos), _p(row_token),
+                             _p(row_weight), _p(x_perm), _p(ws), ws.numel(), _s(stream)),
+           "moe_permute")
+
+
+def moe_grouped_ffn(cfg, x_perm, kept, kept_offsets, row_weight, W_gate, W_up, W_down, y_perm, ws,
+                    stream=None):
+    _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _p(x_perm), _p(kept), _p(kept_offsets),
+                                 _p(row_weight), _p(W_gate), _p(W_up), _p(W_down), _p(y_perm),
+                                 _p(ws), ws.numel(), _s(stream)), "moe_grouped_ffn")
+
+
+def moe_combine(cfg, y_perm, pos, x, Ws_gate, Ws_up, Ws_down, out, ws, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(y_perm), _p(pos), _p(x), _p(Ws_gate),
+                             _p(Ws_up), _p(Ws_down), _p(out), _p(ws), ws.numel(), _s(stream)),
+           "moe_combine")
+
+
+def moe_forward(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, out, ws,
+                stream=None, events=None):
+    if events is None:
+        _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W_gate), _p(W_up),
+                                 _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down), _p(out), _p(ws),
+                                 ws.numel(), _s(stream)), "moe_forward")
+    else:
+        arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check(lib().moe_forward_traced(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W_gate),
+                                        _p(W_up), _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down),
+                                        _p(out), _p(ws), ws.numel(), _s(stream), arr),
+               "moe_forward_traced")
+
+
+def moe_forward_buffers(cfg, ws) -> dict:
+    """Device tensors viewing the intermediates moe_forward leaves in the workspace."""
+    b = MoeBuffers()
+    _check(lib().moe_forward_buffers(ctypes.byref(cfg), _p(ws), ws.numel(), ctypes.byref(b)),
+           "moe_forward_buffers")
+    N, k, E, d = cfg.N, cfg.k, cfg.E, cfg.d
+    R = moe_grouped_rows(cfg)
+    act = torch.bfloat16 if cfg.act_dtype == MOE_BF16 else torch.float32
+    esz = 2 if cfg.act_dtype == MOE_BF16 else 4
+    base = ws.data_ptr()
+
+    def view(ptr, n, dtype, esize):
+        off = ptr - base
+        return ws[off:off + n * esize].view(dtype)
+
+    return dict(
+        idx=view(b.idx, N * k, torch.int32, 4).view(N, k),
+        w=view(b.w, N * k, torch.float32, 4).view(N, k),
+        gap=view(b.gap, N, torch.float32, 4),
+        P_sum=view(b.P_sum, E, torch.float32, 4),
+        counts=view(b.counts, E, torch.int32, 4),
+        offsets=view(b.offsets, E + 1, torch.int32, 4),
+        kept=view(b.kept, E, torch.int32, 4),
+        kept_offsets=view(b.kept_offsets, E + 1, torch.int32, 4),
+        perm=view(b.perm, N * k, torch.int32, 4),
+        pos=view(b.pos, N * k, torch.int32, 4),
+        row_token=view(b.row_token, R, torch.int32, 4),
+        row_weight=view(b.row_weight, R, torch.float32, 4),
+        x_perm=view(b.x_perm, R * d, act, esz).view(R, d),
+        y_perm=view(b.y_perm, R * d, act, esz).view(R, d),
+    )
+
+
+def moe_stats(cfg, counts, kept, P_sum, pos, gap, ws, stream=None):
+    """Returns dict(f, P, aux, dropped, fully_dropped, near_tie, touched_experts, kept_rows,
+    device_error).  Synchronises the stream."""
+    E = cfg.E
+    f = (ctypes.c_float * E)()
+    P = (ctypes.c_float * E)()
+    s = MoeStatsSummary()
+    _check(lib().moe_stats(ctypes.byref(cfg), _p(counts), _p(kept), _p(P_sum), _p(pos), _p(gap),
+                           f, P, ctypes.byref(s), _p(ws), ws.numel(), _s(stream)), "moe_stats")
+    return dict(f=list(f), P=list(P), aux=s.aux, dropped=s.dropped, fully_dropped=s.fully_dropped,
+                near_tie=s.near_tie, touched_experts=s.touched_experts, kept_rows=s.kept_rows,
+                device_error=s.device_error)
+
+
+def moe_device_error(ws, stream=None) -> int:
+    """Synchronises and returns the sticky device error word (MOE_DEVERR_* bits)."""
+    code = ctypes.c_int32(0)
+    lib().moe_device_error(_p(ws), ws.numel(), ctypes.byref(code), _s(stream))
+    return code.value
+
+
+# ------------------------------------------------------------------ convenience
+
+class MoELayer:
+    """Holds device weights, a workspace and an output buffer for one layer shape."""
+
+    def __init__(self, cfg: MoeCfg, weights: dict, device="cuda"):
+        self.cfg = cfg
+        self.w = weights
+        self.device = torch.device(device)
+        self.ws = workspace(cfg, self.device)
+        act = torch.bfloat16 if cfg.act_dtype == MOE_BF16 else torch.float32
+        self.out = torch.empty((cfg.N, cfg.d), dtype=act, device=self.device)
+
+    def forward(self, x: torch.Tensor, stream=None, events=None) -> torch.Tensor:
+        w = self.w
+        moe_forward(self.cfg, x, w["W_r"], w.get("b_r"), w["W_gate"], w["W_up"], w["W_down"],
+                    w.get("Ws_gate"), w.get("Ws_up"), w.get("Ws_down"), self.out, self.ws,
+                    stream, events)
+        return self.out
+
+    def buffers(self) -> dict:
+        return moe_forward_buffers(self.cfg, self.ws)
+
+    def stats(self, stream=None) -> dict:
+        b = self.buffers()
+        return moe_stats(self.cfg, b["counts"], b["kept"], b["P_sum"], b["pos"], b["gap"],
+                         self.ws, stream)
+
+    def device_error(self, stream=None) -> int:
+        return moe_device_error(self.ws, stream)

@@ -1,0 +1,74 @@
+"""GPU parity of moe_grouped_ffn (grouped gate/up SwiGLU GEMM + grouped down GEMM with the
+routing weight applied) through the C ABI.  Row r of expert e must equal
+row_weight[r] * Expert_e(x_perm[r]) as the oracle computes it for one token and one expert.
+Group sizes span several 128-row tiles and ragged tails (1, 127, 128, 129, 300 rows), empty
+experts, d and d_ff that are not multiples of the 64-wide k-blocks or the output tiles."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+import oracle
+from sparse_conditional_moe_b300 import moe
+
+from gpu_util import ExpertCache, compare_rows, dtype_code, out_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _grouped(spec, rows_per_expert, seed=0):
+    E = spec.E
+    L = moe_synth.make_layer(spec.with_(N=1), seed=seed)
+    R = int(sum(rows_per_expert))
+    g = torch.Generator().manual_seed(seed + 1)
+    act = torch.bfloat16 if spec.dtype == "bf16" else torch.float32
+    x_perm = torch.randn((max(R, 1), spec.d), generator=g).to(act)
+    row_w = torch.rand((max(R, 1),), generator=g)
+    kept = torch.tensor(rows_per_expert, dtype=torch.int32)
+    kept_off = torch.zeros(E + 1, dtype=torch.int32)
+    kept_off[1:] = torch.cumsum(kept, 0)
+    # a config whose grouped-row capacity covers R rows
+    cfg = moe.make_cfg(N=max(R, 1), d=spec.d, d_ff=spec.d_ff, E=E, k=1,
+                       act_dtype=moe.MOE_BF16 if spec.dtype == "bf16" else moe.MOE_F32)
+    ws = moe.workspace(cfg)
+    dev = {n: L[n].cuda() for n in ("W_gate", "W_up", "W_down")}
+    y = torch.empty((max(R, 1), spec.d), dtype=act, device="cuda")
+    moe.moe_grouped_ffn(cfg, x_perm.cuda(), kept.cuda(), kept_off.cuda(), row_w.cuda(),
+                        dev["W_gate"], dev["W_up"], dev["W_down"], y, ws)
+    assert moe.moe_device_error(ws) == 0
+    # oracle: one expert, one token, weight row_w[r]
+    cache = ExpertCache(dev)
+    code = dtype_code(spec)
+    ref = np.zeros((R, spec.d))
+    for e in range(E):
+        for r in range(int(kept_off[e]), int(kept_off[e + 1])):
+            o = oracle.moe_token(x_perm[r], np.array([row_w[r]], np.float32), np.array([1]),
+                                 [cache.routed(e)], [], code, 1 if code == oracle.BF16 else 0)
+            ref[r] = out_f64(o, spec)
+    return out_f64(y[:R], spec), ref
+
+
+@pytest.mark.parametrize("d,F,rows", [
+    (256, 384, [1, 127, 128, 129, 300, 0]),       # several m-tiles, ragged, empty expert
+    (520, 200, [5, 0, 131, 64]),                    # ragged k-block, ragged n-tiles
+    (128, 128, [128]),                              # exactly one tile
+    (1024, 1024, [256, 257, 3]),
+])
+def test_grouped_ffn_bf16(d, F, rows):
+    spec = moe_synth.LayerSpec("g", N=1, d=d, d_ff=F, E=len(rows), k=1)
+    got, ref = _grouped(spec, rows, seed=d + F)
+    compare_rows(got, ref, spec, what="grouped ffn")
+
+
+@pytest.mark.parametrize("d,F,rows", [(128, 256, [16, 0, 65, 1]), (36, 20, [3, 70])])
+def test_grouped_ffn_fp32(d, F, rows):
+    spec = moe_synth.LayerSpec("g", N=1, d=d, d_ff=F, E=len(rows), k=1, dtype="f32")
+    got, ref = _grouped(spec, rows, seed=d)
+    compare_rows(got, ref, spec, what="grouped ffn fp32")
+
+
+def test_grouped_ffn_long_reduction():
+    """K = 7168 (112 k-blocks through the 4-stage ring) on a few rows of two experts."""
+    spec = moe_synth.LayerSpec("g", N=1, d=7168, d_ff=256, E=2, k=1)
+    got, ref = _grouped(spec, [130, 7], seed=5)
+    compare_rows(got, ref, spec, what="grouped ffn K=7168")

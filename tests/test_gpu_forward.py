@@ -1,0 +1,142 @@
+"""End-to-end GPU parity of moe_forward against the oracle, through the C ABI.
+
+Small layers (the oracle finishes in seconds) are compared on every token: routing bit-exact
+(near-ties excluded), counts / offsets / permutation / positions bit-exact, outputs within the
+stated tolerance.  The five workload layers are compared at their full sizes in the launch
+configuration the benchmark uses: routing and grouping on every token, outputs on a seeded
+sample of tokens the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+import oracle
+from sparse_conditional_moe_b300 import moe
+
+from gpu_util import (ExpertCache, check_routing, compare_rows, dtype_code, oracle_tokens,
+                      out_f64, run_layer, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    moe_synth.TINY,
+    moe_synth.PAGE_SELFTEST,
+    moe_synth.LayerSpec("bf16_small", N=300, d=256, d_ff=384, E=8, k=2, n_shared=1,
+                        d_ff_shared=128),
+    moe_synth.LayerSpec("bf16_many_experts", N=200, d=512, d_ff=256, E=64, k=6),
+    moe_synth.LayerSpec("bf16_capacity", N=600, d=256, d_ff=128, E=16, k=4,
+                        capacity_factor=0.6, zipf_bias=1.2, n_shared=1, d_ff_shared=64),
+    moe_synth.LayerSpec("bf16_capacity_no_shared", N=400, d=128, d_ff=256, E=8, k=2,
+                        capacity_factor=0.25, zipf_bias=2.0),
+    moe_synth.LayerSpec("bf16_k1", N=129, d=192, d_ff=136, E=4, k=1),
+    moe_synth.LayerSpec("bf16_dense_k_eq_E", N=70, d=128, d_ff=128, E=4, k=4, n_shared=2,
+                        d_ff_shared=64),
+    moe_synth.LayerSpec("f32_capacity", N=100, d=64, d_ff=96, E=8, k=3, capacity_factor=0.5,
+                        dtype="f32", n_shared=1, d_ff_shared=32),
+]
+
+
+def _grouping_checks(spec, bufs, idx_o, differs):
+    cap = oracle.capacity(spec.N, spec.k, spec.E, spec.capacity_factor)
+    ref = oracle.permute(idx_o, spec.E, cap)
+    if differs.size:          # a near-tie token went to another expert: grouping not unique
+        return ref
+    for key in ("counts", "offsets", "kept", "kept_offsets"):
+        assert np.array_equal(bufs[key].cpu().numpy(), ref[key]), key
+    assert np.array_equal(bufs["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(bufs["pos"].cpu().numpy(), ref["pos"])
+    return ref
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
+def test_forward_small_layers_every_token(spec):
+    L = moe_synth.make_layer(spec, seed=11)
+    dev = to_dev(L)
+    lay, out = run_layer(spec, dev)
+    assert lay.device_error() == 0
+    bufs = lay.buffers()
+    code = dtype_code(spec)
+    ref, ex = oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor)
+    excl, differs = check_routing(bufs["idx"].cpu().numpy(), bufs["w"].cpu().numpy(),
+                                  bufs["gap"].cpu().numpy(), ex["idx"], ex["w"], ex["probs"],
+                                  ex["gap"])
+    _grouping_checks(spec, bufs, ex["idx"], differs)
+    rows = np.ones(spec.N, bool) if differs.size == 0 else ~excl
+    compare_rows(out_f64(out, spec), out_f64(ref, spec), spec, rows=rows)
+    # fully dropped tokens without shared experts are exactly zero
+    if spec.capacity_factor > 0 and spec.n_shared == 0:
+        dropped = ex["keep"].sum(1) == 0
+        assert dropped.any()
+        assert torch.all(out[torch.from_numpy(dropped).cuda()] == 0)
+
+
+def test_forward_is_deterministic_and_repeatable():
+    spec = SMALL[4]
+    dev = to_dev(moe_synth.make_layer(spec, seed=2))
+    lay, out1 = run_layer(spec, dev)
+    out2 = lay.forward(dev["x"]).clone()
+    out3 = lay.forward(dev["x"]).clone()
+    assert torch.equal(out1, out2) and torch.equal(out2, out3)
+
+
+def test_forward_empty_batch():
+    spec = moe_synth.LayerSpec("empty", N=0, d=128, d_ff=128, E=8, k=2, n_shared=1,
+                               d_ff_shared=128)
+    dev = to_dev(moe_synth.make_layer(spec.with_(N=4), seed=0))
+    dev["x"] = dev["x"][:0]
+    lay, out = run_layer(spec, dev)
+    assert out.shape == (0, 128) and lay.device_error() == 0
+
+
+def test_stats_match_oracle():
+    spec = SMALL[4]
+    L = moe_synth.make_layer(spec, seed=4)
+    lay, out = run_layer(spec, to_dev(L))
+    st = lay.stats()
+    ref, ex = oracle.forward_naive(L, spec.k, dtype_code(spec), cf=spec.capacity_factor)
+    so = oracle.stats(ex["idx"], ex["probs"], ex["keep"], ex["gap"])
+    np.testing.assert_allclose(st["f"], so["f"], rtol=0, atol=1e-7)
+    np.testing.assert_allclose(st["P"], so["P"], rtol=1e-5, atol=1e-7)
+    assert abs(st["aux"] - so["aux"]) <= 1e-5 * max(1.0, so["aux"])
+    assert st["dropped"] == so["dropped"] and st["fully_dropped"] == so["fully_dropped"]
+    assert st["near_tie"] == so["near_tie"] and st["device_error"] == 0
+    assert st["kept_rows"] == int(ex["keep"].sum())
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+FULL = [moe_synth.TINY, moe_synth.MIXTRAL, moe_synth.DSV3_PREFILL, moe_synth.DSV3_DECODE,
+        moe_synth.QWEN3_SKEWED]
+
+
+@pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
+def test_forward_full_size_workloads(spec):
+    torch.cuda.empty_cache()
+    dev = moe_synth.make_layer(spec, seed=0, device="cuda")
+    lay, out = run_layer(spec, dev)
+    assert lay.device_error() == 0
+    bufs = lay.buffers()
+    x_host = dev["x"].cpu()
+    b_host = None if dev["b_r"] is None else dev["b_r"].cpu()
+    code = dtype_code(spec)
+    idx_o, w_o, probs_o, gap_o = oracle.route(x_host, dev["W_r"].cpu(), b_host, spec.k, code)
+    excl, differs = check_routing(bufs["idx"].cpu().numpy(), bufs["w"].cpu().numpy(),
+                                  bufs["gap"].cpu().numpy(), idx_o, w_o, probs_o, gap_o)
+    _grouping_checks(spec, bufs, idx_o, differs)
+    cap = oracle.capacity(spec.N, spec.k, spec.E, spec.capacity_factor)
+    keep_o = oracle.keep_naive(idx_o, spec.E, cap)
+    if spec.capacity_factor > 0:
+        assert keep_o.min() == 0       # the skewed layer really overflows some experts
+    n_sample = {"tiny_fp32": 64, "deepseek_v3_decode_bf16": 24}.get(spec.name, 12)
+    tok = moe_synth.sample_tokens(spec.N, n_sample, seed=1).numpy()
+    tok = tok[~excl[tok]] if differs.size else tok
+    if spec.capacity_factor > 0:       # include tokens that lost assignments
+        lost = np.nonzero(keep_o.sum(1) < spec.k)[0]
+        tok = np.unique(np.concatenate([tok, lost[:: max(1, lost.size // 6)][:6]]))
+    cache = ExpertCache(dev)
+    ref = oracle_tokens(spec, x_host, tok, idx_o, w_o, keep_o, cache)
+    got = out_f64(out[torch.from_numpy(tok).cuda()], spec)
+    compare_rows(got, ref, spec, what=spec.name)
+    del dev, lay, out
+    torch.cuda.empty_cache()
