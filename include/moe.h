@@ -69,7 +69,7 @@ typedef struct {
     int32_t k;                /* experts per token, 1..min(E, 16) */
     int32_t n_shared;         /* shared experts S, 0..8 (always active, weight 1) */
     int32_t d_ff_shared;      /* shared expert hidden dim F_s (ignored when S = 0) */
-    float capacity_factor;    /* <= 0: no capacity limit; else C = ceil(CF * N * k / E) */
+    double capacity_factor;   /* <= 0: no capacity limit; else C = ceil(CF * N * k / E) in fp64 */
     int32_t renorm;           /* 1: renormalise the k weights to sum to 1 (the pages' form) */
     int32_t bias_mode;        /* 0: no router bias; 1: b_r added to the logits before softmax */
     int32_t act_dtype;        /* moe_dtype */

@@ -22,7 +22,7 @@ int device_sm_count() {
 
 int64_t capacity(const moe_cfg& c) {
     if (!(c.capacity_factor > 0.f)) return -1;
-    return (int64_t)ceil((double)c.capacity_factor * (double)c.N * (double)c.k / (double)c.E);
+    return (int64_t)ceil(c.capacity_factor * (double)c.N * (double)c.k / (double)c.E);
 }
 
 int64_t grouped_rows(const moe_cfg& c) {

@@ -5,8 +5,10 @@
 // and the k weights divided by their sum.  The router stays fp32 end to end.
 //
 // One block = BT tokens x all E experts.  The d-loop stages a DK-wide slice of x (widened to
-// fp32) and of W_r in shared memory; every thread accumulates a TT x TE register tile in
-// increasing-d order with fp32 FMA.  The logits then go through shared memory to the
+// fp32) and of W_r in shared memory; every thread computes a TT x TE register tile, each slice
+// as an fp32 FMA chain in increasing-d order, slices added to the running logit with
+// compensated (Kahan) summation, so the logit error stays near u*sqrt(DK) for any d.  The
+// logits then go through shared memory to the
 // epilogue, where each warp owns whole tokens: max / sum by warp shuffles, top-k by k rounds
 // of a warp arg-max on (probability desc, expert index asc), the (k+1)-th for the near-tie
 // gap, and per-block column sums of the probabilities (deterministic, no float atomics).
@@ -70,11 +72,13 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
     const int tx = tid % TEn, ty = tid / TEn;
     const int64_t t0 = (int64_t)blockIdx.x * BT;
 
-    float acc[TT][TE];
+    // acc: running logit; cmp: its compensation term (Kahan), so that the only rounding left
+    // of any size is inside each DK-long slice (fp32 FMA chain over DK products).
+    float acc[TT][TE], cmp[TT][TE];
 #pragma unroll
     for (int i = 0; i < TT; i++)
 #pragma unroll
-        for (int j = 0; j < TE; j++) acc[i][j] = 0.f;
+        for (int j = 0; j < TE; j++) acc[i][j] = cmp[i][j] = 0.f;
 
     for (int k0 = 0; k0 < d; k0 += DK) {
         // stage x[t0 .. t0+BT) x [k0 .. k0+DK) as fp32 (zero outside the batch / past d)
@@ -93,6 +97,11 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
             Ws[kk * EP + e] = val;
         }
         __syncthreads();
+        float part[TT][TE];
+#pragma unroll
+        for (int i = 0; i < TT; i++)
+#pragma unroll
+            for (int j = 0; j < TE; j++) part[i][j] = 0.f;
 #pragma unroll 4
         for (int kk = 0; kk < DK; kk++) {
             float xv[TT], wv[TE];
@@ -103,8 +112,17 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
 #pragma unroll
             for (int i = 0; i < TT; i++)
 #pragma unroll
-                for (int j = 0; j < TE; j++) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+                for (int j = 0; j < TE; j++) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
         }
+#pragma unroll
+        for (int i = 0; i < TT; i++)
+#pragma unroll
+            for (int j = 0; j < TE; j++) {
+                const float y = part[i][j] - cmp[i][j];
+                const float t = acc[i][j] + y;
+                cmp[i][j] = (t - acc[i][j]) - y;
+                acc[i][j] = t;
+            }
         __syncthreads();
     }
 

