@@ -127,6 +127,26 @@ MOE_API moe_status moe_permute(const moe_cfg *cfg, const int32_t *idx, const flo
                        void *x_perm, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute without a workspace, for callers that cannot allocate
+ * device memory where they run this step (a plugin interface with no workspace argument, or a
+ * process whose device memory belongs to another allocator, where a cudaMalloc mid-run would
+ * fail under fragmentation or synchronise the device).  Nothing in the pages corresponds to
+ * this call: it is an interface convenience around the same grouping kernels.
+ * Same arguments and results as moe_permute, except:
+ *   - no ws / ws_bytes: the per-block tables live in a fixed 1 MiB array inside the library
+ *     (held by every GPU that loads it until exit), which caps ceil(N*k / 2048) * E at 131072;
+ *     larger calls return MOE_ERR_WORKSPACE.  The call allocates nothing.
+ *   - err [1] int32, nullable, device: MOE_DEVERR_* bits are OR-ed into it (caller clears it).
+ *   - all calls share the array: calls that overlap on the GPU race.  The first call on each
+ *     device looks up the array's address; make it before any stream capture.
+ */
+MOE_API moe_status moe_permute_noalloc(const moe_cfg *cfg, const int32_t *idx, const float *w,
+                                       const void *x, int32_t *counts, int32_t *offsets,
+                                       int32_t *kept, int32_t *kept_offsets, int32_t *perm,
+                                       int32_t *pos, int32_t *row_token, float *row_weight,
+                                       void *x_perm, int32_t *err, void *stream);
+
+/*
  * moe_grouped_ffn -- every routed expert's SwiGLU FFN on its grouped rows as grouped GEMMs
  * ("混合专家 MoE", 实现 section: after grouping, a single grouped GEMM serves all experts;
  * Expert.forward):

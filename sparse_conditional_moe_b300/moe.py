@@ -22,8 +22,9 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 # Every function the header declares (checked against the library's exports by the tests).
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_route",
-           "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_forward", "moe_forward_traced",
-           "moe_forward_buffers", "moe_stats", "moe_device_error", "moe_status_string")
+           "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
+           "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
+           "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -71,6 +72,7 @@ def lib():
             "moe_workspace_init": [C, P, SZ, P],
             "moe_route": [C, P, P, P, P, P, P, P, P, SZ, P],
             "moe_permute": [C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_permute_noalloc": [C, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
             "moe_grouped_ffn": [C, P, P, P, P, P, P, P, P, P, SZ, P],
             "moe_combine": [C, P, P, P, P, P, P, P, P, SZ, P],
             "moe_forward": [C, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
@@ -167,6 +169,17 @@ def moe_permute(cfg, idx, w, x, counts, offsets, kept, kept_offsets, perm, pos, 
                              _p(kept), _p(kept_offsets), _p(perm), _p(pos), _p(row_token),
                              _p(row_weight), _p(x_perm), _p(ws), ws.numel(), _s(stream)),
            "moe_permute")
+
+
+def moe_permute_noalloc(cfg, idx, w, x, counts, offsets, kept, kept_offsets, perm, pos,
+                        row_token, row_weight, x_perm, err=None, stream=None):
+    """moe_permute for callers that cannot provide a workspace: the library keeps the per-block
+    tables in a fixed device array of its own (see include/moe.h for its size limit and the
+    rule that overlapping calls race on it)."""
+    _check(lib().moe_permute_noalloc(ctypes.byref(cfg), _p(idx), _p(w), _p(x), _p(counts),
+                                     _p(offsets), _p(kept), _p(kept_offsets), _p(perm), _p(pos),
+                                     _p(row_token), _p(row_weight), _p(x_perm), _p(err),
+                                     _s(stream)), "moe_permute_noalloc")
 
 
 def moe_grouped_ffn(cfg, x_perm, kept, kept_offsets, row_weight, W_gate, W_up, W_down, y_perm, ws,
