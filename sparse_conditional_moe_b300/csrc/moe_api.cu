@@ -47,7 +47,10 @@ WsLayout ws_layout(const moe_cfg& c) {
     const int64_t S = c.n_shared, F = c.d_ff, Fs = c.d_ff_shared, d = c.d;
     const size_t esz = c.act_dtype == MOE_BF16 ? 2 : 4;
     L.err = take(256);
-    L.p_part = take(4 * (size_t)router_blocks(N, (int)E) * E);
+    L.p_part = take(4 * (size_t)router_part_rows(N) * E);
+    const bool tc_router = router_uses_tensor_cores(c);
+    L.router_w3 = take(tc_router ? 2 * 3 * (size_t)E * d : 0);
+    L.logits = take(tc_router ? 4 * (size_t)N * E : 0);
     L.blk_hist = take(4 * (size_t)perm_blocks(A) * E);
     L.blk_base = take(4 * (size_t)perm_blocks(A) * E);
     L.mtile_off = take(4 * (size_t)(E + 1));
@@ -271,7 +274,8 @@ moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const 
     if (cfg->bias_mode == 1) MOE_TRY(need(b_r, 4));
     const WsLayout L = ws_layout(*cfg);
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.p_part), P_sum,
-                           (cudaStream_t)stream));
+                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits),
+                           at<int32_t>(ws, L.err), (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -357,7 +361,8 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
-                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum), s));
+                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum),
+                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
                             at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),

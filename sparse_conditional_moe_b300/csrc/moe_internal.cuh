@@ -11,9 +11,9 @@ namespace moe {
 
 // ------------------------------------------------------------------ router tiling
 
-// Tokens per router block for a padded expert count (see router.cu).
-int router_block_tokens(int E);
-int router_blocks(int64_t N, int E);
+// Router path selection and the rows of its per-block probability sums (an upper bound).
+bool router_uses_tensor_cores(const moe_cfg& c);
+int64_t router_part_rows(int64_t N);
 
 // ------------------------------------------------------------------ permute tiling
 
@@ -28,7 +28,9 @@ inline int perm_blocks(int64_t slots) {
 
 struct WsLayout {
     size_t err;          // int32 [64]: [0] sticky error word, [8..15] stats counters
-    size_t p_part;       // float [router_blocks * E]
+    size_t p_part;       // float [router_part_rows(N) * E]
+    size_t router_w3;    // bf16 [3, E, d]: exact hi/mid/lo split of W_r (tensor-core router)
+    size_t logits;       // float [N, E] (tensor-core router)
     size_t blk_hist;     // int32 [perm_blocks * E]
     size_t blk_base;     // int32 [perm_blocks * E]
     size_t mtile_off;    // int32 [E + 1]: m-tile prefix of the routed grouped GEMMs
@@ -49,7 +51,11 @@ WsLayout ws_layout(const moe_cfg& c);
 
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* p_part, float* P_sum,
-                          cudaStream_t s);
+                          __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s);
+
+// Tensor-core router logits [N, E] (fp32) for bf16 x (see router_tc.cu).
+cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
+                             __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s);
 
 cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w, const void* x,
                            int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_off,

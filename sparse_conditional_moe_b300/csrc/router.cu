@@ -1,17 +1,22 @@
-// router.cu -- fused router: logits (fp32 CUDA-core GEMM) + softmax + top-k + renormalise.
+// router.cu -- router: logits, softmax over all experts, top-k, renormalisation.
 //
 // Page "混合专家 MoE", section "实现：逐 token 与按专家分组", MoE.route: a linear layer d -> E
 // scores every expert, softmax over the E scores, the k largest kept in descending order,
-// and the k weights divided by their sum.  The router stays fp32 end to end.
+// and the k weights divided by their sum.  The router stays fp32 end to end: the logits are
+// fp32 sums of exact products, and the top-k decision is taken on fp32 probabilities.
 //
-// One block = BT tokens x all E experts.  The d-loop stages a DK-wide slice of x (widened to
-// fp32) and of W_r in shared memory; every thread computes a TT x TE register tile, each slice
-// as an fp32 FMA chain in increasing-d order, slices added to the running logit with
-// compensated (Kahan) summation, so the logit error stays near u*sqrt(DK) for any d.  The
-// logits then go through shared memory to the
-// epilogue, where each warp owns whole tokens: max / sum by warp shuffles, top-k by k rounds
-// of a warp arg-max on (probability desc, expert index asc), the (k+1)-th for the near-tie
-// gap, and per-block column sums of the probabilities (deterministic, no float atomics).
+// Three ways to get the logits, one epilogue:
+//   E <= 32      router_gemv_kernel: a warp per two tokens, lanes split d in 8-wide chunks,
+//                each lane accumulates E short fp32 chains, a butterfly shuffle sums them;
+//   E > 32, bf16 the tensor-core router of router_tc.cu writes fp32 logits [N, E], then
+//                logits_topk_kernel finishes each token;
+//   E > 32, fp32 router_tiled_kernel: BT tokens x all experts per block, DK-wide slices of x
+//                and W_r in shared memory, each slice an fp32 FMA chain, slices added to the
+//                running logit with compensated (Kahan) summation.
+// finish_token() is the common epilogue: each warp owns a token, lane l holds the logits of
+// experts l, l+32, ...; max and sum by warp shuffles; top-k by k rounds of a warp arg-max on
+// (probability desc, expert index asc); the (k+1)-th gives the near-tie gap; per-block column
+// sums of the probabilities go to p_part (deterministic, no float atomics).
 #include <float.h>
 #include <limits.h>
 
@@ -21,21 +26,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouterThreads = 256;
-
-template <int EP>
-struct RouterTile {
-    static constexpr int TE_THREADS = EP < 32 ? EP : 32;                  // threads along experts
-    static constexpr int TE = EP / TE_THREADS;                            // experts per thread
-    static constexpr int TT_THREADS = kRouterThreads / TE_THREADS;        // threads along tokens
-    static constexpr int TT = EP >= 1024 ? 1 : (EP >= 512 ? 2 : (EP >= 16 ? 4 : 2));
-    static constexpr int BT = TT_THREADS * TT;                            // tokens per block
-    static constexpr int DK = EP >= 1024 ? 8 : (EP >= 512 ? 16 : 32);     // d-slice per stage
-    static constexpr int XS = BT * (DK + 1);                              // x slice [BT][DK+1]
-    static constexpr int WS = DK * EP;                                    // W slice [DK][EP]
-    static constexpr int LS = BT * (EP + 1);                              // logits [BT][EP+1]
-    static constexpr int SMEM_FLOATS = (XS + WS) > LS ? (XS + WS) : LS;
-    static constexpr int NV = EP >= 32 ? EP / 32 : 1;                     // values per lane
-};
+constexpr int kWarps = kRouterThreads / 32;
 
 __device__ __forceinline__ float load_x(const float* x, int64_t i) { return x[i]; }
 __device__ __forceinline__ float load_x(const __nv_bfloat16* x, int64_t i) {
@@ -55,21 +46,249 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// Softmax, top-k, gap and renormalisation of one token held by one warp.  v[i] is the logit of
+// expert lane + 32 i (ignored for experts >= E).  Adds the probabilities into pacc.
+template <int NV>
+__device__ __forceinline__ void finish_token(float (&v)[NV], const float* __restrict__ b_r, int E,
+                                             int k, int renorm, int64_t tok,
+                                             int32_t* __restrict__ idx_out,
+                                             float* __restrict__ w_out,
+                                             float* __restrict__ gap_out, float (&pacc)[NV]) {
+    const int lane = threadIdx.x & 31;
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            if (b_r) v[i] += b_r[e];
+            m = fmaxf(m, v[i]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? expf(v[i] - m) : 0.f;
+        s += v[i];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? v[i] / s : -1.f;   // -1: never selected
+        if (e < E) pacc[i] += v[i];
+    }
+    uint32_t taken = 0;
+    float my_val = 0.f, kth = 0.f, sel_sum = 0.f;
+    int my_idx = 0;
+    const int rounds = k < E ? k + 1 : k;
+    for (int j = 0; j < rounds; j++) {
+        float bv = -2.f;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int e = lane + 32 * i;
+            if (!(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+        warp_argmax(bv, bi);
+        if (j < k) {
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == j) {
+                my_val = bv;
+                my_idx = bi;
+            }
+            sel_sum += bv;   // slot order, identical on every lane
+            kth = bv;
+        } else if (lane == 0 && gap_out) {
+            gap_out[tok] = kth - bv;
+        }
+    }
+    if (k >= E && lane == 0 && gap_out) gap_out[tok] = __int_as_float(0x7f800000);
+    if (lane < k) {
+        idx_out[tok * k + lane] = my_idx;
+        w_out[tok * k + lane] = renorm ? my_val / sel_sum : my_val;
+    }
+}
+
+// Column sums of the probabilities of this block's tokens, combined across warps in warp order.
+template <int NV>
+__device__ __forceinline__ void write_p_part(const float (&pacc)[NV], float* sm /*[kWarps][32NV]*/,
+                                             int E, float* __restrict__ p_part) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int EPW = 32 * NV;
+#pragma unroll
+    for (int i = 0; i < NV; i++) sm[warp * EPW + lane + 32 * i] = pacc[i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRouterThreads) {
+        float sacc = 0.f;
+        for (int w = 0; w < kWarps; w++) sacc += sm[w * EPW + e];
+        p_part[(int64_t)blockIdx.x * E + e] = sacc;
+    }
+}
+
+// ------------------------------------------------------------------ E <= 32: GEMV
+
+constexpr int kGemvTokensPerWarp = 2;
+constexpr int kGemvTokensPerBlock = kWarps * kGemvTokensPerWarp;
+
+template <typename T>
+struct Chunk8;
+template <>
+struct Chunk8<__nv_bfloat16> {
+    __device__ static void load(const __nv_bfloat16* p, float (&f)[8]) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+};
+template <>
+struct Chunk8<float> {
+    __device__ static void load(const float* p, float (&f)[8]) {
+        float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+};
+
 template <int EP, typename T>
 __global__ void __launch_bounds__(kRouterThreads)
-router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b_r,
-              int64_t N, int d, int E, int k, int renorm, int32_t* __restrict__ idx_out,
-              float* __restrict__ w_out, float* __restrict__ gap_out, float* __restrict__ p_part) {
+router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
+                   const float* __restrict__ b_r, int64_t N, int d, int E, int k, int renorm,
+                   int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                   float* __restrict__ gap_out, float* __restrict__ p_part) {
+    __shared__ float sm[kWarps * 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)blockIdx.x * kGemvTokensPerBlock + warp * kGemvTokensPerWarp;
+    float pacc[1] = {0.f};
+    float acc[kGemvTokensPerWarp][EP];
+#pragma unroll
+    for (int t = 0; t < kGemvTokensPerWarp; t++)
+#pragma unroll
+        for (int e = 0; e < EP; e++) acc[t][e] = 0.f;
+    bool live[kGemvTokensPerWarp];
+#pragma unroll
+    for (int t = 0; t < kGemvTokensPerWarp; t++) live[t] = t0 + t < N;
+    const int d8 = d & ~7;
+    for (int c = lane * 8; c < d8; c += 256) {
+        float xv[kGemvTokensPerWarp][8];
+#pragma unroll
+        for (int t = 0; t < kGemvTokensPerWarp; t++) {
+            if (live[t]) Chunk8<T>::load(x + (t0 + t) * d + c, xv[t]);
+            else
+#pragma unroll
+                for (int i = 0; i < 8; i++) xv[t][i] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < EP; e++) {
+            if (e < E) {
+                float wv[8];
+                Chunk8<float>::load(W_r + (int64_t)e * d + c, wv);
+#pragma unroll
+                for (int t = 0; t < kGemvTokensPerWarp; t++)
+#pragma unroll
+                    for (int i = 0; i < 8; i++) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
+            }
+        }
+    }
+    for (int c = d8 + lane; c < d; c += 32) {   // d not a multiple of 8 (fp32 layers)
+#pragma unroll
+        for (int e = 0; e < EP; e++) {
+            if (e < E) {
+                const float wv = W_r[(int64_t)e * d + c];
+#pragma unroll
+                for (int t = 0; t < kGemvTokensPerWarp; t++)
+                    if (live[t]) acc[t][e] = fmaf(load_x(x, (t0 + t) * d + c), wv, acc[t][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kGemvTokensPerWarp; t++) {
+#pragma unroll
+        for (int e = 0; e < EP; e++)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], off);
+        if (!live[t]) continue;    // warp-uniform
+        float v[1] = {0.f};
+#pragma unroll
+        for (int e = 0; e < EP; e++)
+            if (e == lane) v[0] = acc[t][e];
+        finish_token<1>(v, b_r, E, k, renorm, t0 + t, idx_out, w_out, gap_out, pacc);
+    }
+    write_p_part<1>(pacc, sm, E, p_part);
+}
+
+// ------------------------------------------------------------------ logits -> top-k
+
+constexpr int kTopkTokensPerBlock = 32;
+
+template <int NV>
+__global__ void __launch_bounds__(kRouterThreads)
+logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b_r, int64_t N,
+                   int E, int k, int renorm, int32_t* __restrict__ idx_out,
+                   float* __restrict__ w_out, float* __restrict__ gap_out,
+                   float* __restrict__ p_part) {
+    __shared__ float sm[kWarps * 32 * NV];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float pacc[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) pacc[i] = 0.f;
+    for (int t = warp; t < kTopkTokensPerBlock; t += kWarps) {
+        const int64_t tok = (int64_t)blockIdx.x * kTopkTokensPerBlock + t;
+        if (tok >= N) break;
+        float v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? logits[tok * E + e] : 0.f;
+        }
+        finish_token<NV>(v, b_r, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
+    }
+    write_p_part<NV>(pacc, sm, E, p_part);
+}
+
+// ------------------------------------------------------------------ E > 32, fp32: tiled
+
+template <int EP>
+struct RouterTile {
+    static constexpr int TE = EP / 32;                                    // experts per thread
+    static constexpr int TT = EP >= 1024 ? 1 : (EP >= 512 ? 2 : 4);       // tokens per thread
+    static constexpr int BT = kWarps * TT;                                // tokens per block
+    static constexpr int DK = EP >= 1024 ? 8 : (EP >= 512 ? 16 : 32);     // d-slice per stage
+    static constexpr int XS = BT * (DK + 1);                              // x slice [BT][DK+1]
+    static constexpr int WS = DK * EP;                                    // W slice [DK][EP]
+    static constexpr int LS = BT * (EP + 1);                              // logits [BT][EP+1]
+    static constexpr int SMEM_FLOATS = (XS + WS) > LS ? (XS + WS) : LS;
+    static constexpr int NV = EP / 32;
+};
+
+template <int EP, typename T>
+__global__ void __launch_bounds__(kRouterThreads)
+router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
+                    const float* __restrict__ b_r, int64_t N, int d, int E, int k, int renorm,
+                    int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                    float* __restrict__ gap_out, float* __restrict__ p_part) {
     using Tl = RouterTile<EP>;
-    constexpr int TT = Tl::TT, TE = Tl::TE, BT = Tl::BT, DK = Tl::DK;
-    constexpr int TEn = Tl::TE_THREADS, TTn = Tl::TT_THREADS, NV = Tl::NV;
-    static_assert(Tl::SMEM_FLOATS >= (kRouterThreads / 32) * EP, "P table must fit the staging buffer");
+    constexpr int TT = Tl::TT, TE = Tl::TE, BT = Tl::BT, DK = Tl::DK, NV = Tl::NV;
+    static_assert(Tl::SMEM_FLOATS >= kWarps * EP, "P table must fit the staging buffer");
     __shared__ float sm[Tl::SMEM_FLOATS];
     float* Xs = sm;             // [BT][DK+1]
     float* Ws = sm + Tl::XS;    // [DK][EP]
 
     const int tid = threadIdx.x;
-    const int tx = tid % TEn, ty = tid / TEn;
+    const int tx = tid % 32, ty = tid / 32;
     const int64_t t0 = (int64_t)blockIdx.x * BT;
 
     // acc: running logit; cmp: its compensation term (Kahan), so that the only rounding left
@@ -81,17 +300,15 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
         for (int j = 0; j < TE; j++) acc[i][j] = cmp[i][j] = 0.f;
 
     for (int k0 = 0; k0 < d; k0 += DK) {
-        // stage x[t0 .. t0+BT) x [k0 .. k0+DK) as fp32 (zero outside the batch / past d)
         for (int v = tid; v < BT * DK; v += kRouterThreads) {
-            int t = v / DK, kk = v % DK;
-            int64_t tok = t0 + t;
+            const int t = v / DK, kk = v % DK;
+            const int64_t tok = t0 + t;
             float val = 0.f;
             if (tok < N && k0 + kk < d) val = load_x(x, tok * d + k0 + kk);
             Xs[t * (DK + 1) + kk] = val;
         }
-        // stage W_r[0 .. EP) x [k0 .. k0+DK) transposed to [DK][EP] (zero for padded experts)
         for (int v = tid; v < EP * DK; v += kRouterThreads) {
-            int e = v % EP, kk = v / EP;
+            const int e = v % EP, kk = v / EP;
             float val = 0.f;
             if (e < E && k0 + kk < d) val = W_r[(int64_t)e * d + k0 + kk];
             Ws[kk * EP + e] = val;
@@ -106,9 +323,9 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
         for (int kk = 0; kk < DK; kk++) {
             float xv[TT], wv[TE];
 #pragma unroll
-            for (int i = 0; i < TT; i++) xv[i] = Xs[(ty + i * TTn) * (DK + 1) + kk];
+            for (int i = 0; i < TT; i++) xv[i] = Xs[(ty + i * kWarps) * (DK + 1) + kk];
 #pragma unroll
-            for (int j = 0; j < TE; j++) wv[j] = Ws[kk * EP + tx + j * TEn];
+            for (int j = 0; j < TE; j++) wv[j] = Ws[kk * EP + tx + j * 32];
 #pragma unroll
             for (int i = 0; i < TT; i++)
 #pragma unroll
@@ -126,110 +343,33 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ W_r, const floa
         __syncthreads();
     }
 
-    // logits -> shared [BT][EP+1]
+    // logits -> shared [BT][EP+1]; thread (ty, tx) owns tokens ty + i*8 and experts tx + j*32
     float* Ls = sm;
 #pragma unroll
     for (int i = 0; i < TT; i++)
 #pragma unroll
-        for (int j = 0; j < TE; j++) Ls[(ty + i * TTn) * (EP + 1) + tx + j * TEn] = acc[i][j];
+        for (int j = 0; j < TE; j++) Ls[(ty + i * kWarps) * (EP + 1) + tx + j * 32] = acc[i][j];
     __syncthreads();
 
-    const int warp = tid / 32, lane = tid % 32;
-    constexpr int kWarps = kRouterThreads / 32;
+    const int warp = tid >> 5, lane = tid & 31;
     float pacc[NV];
 #pragma unroll
     for (int i = 0; i < NV; i++) pacc[i] = 0.f;
-
     for (int t = warp; t < BT; t += kWarps) {
         const int64_t tok = t0 + t;
         if (tok >= N) break;
         float v[NV];
-        float m = -FLT_MAX;
 #pragma unroll
-        for (int i = 0; i < NV; i++) {
-            int e = lane + 32 * i;
-            if (e < E) {
-                float l = Ls[t * (EP + 1) + e];
-                if (b_r) l += b_r[e];
-                v[i] = l;
-                m = fmaxf(m, l);
-            } else {
-                v[i] = -FLT_MAX;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            int e = lane + 32 * i;
-            v[i] = (e < E) ? expf(v[i] - m) : 0.f;
-            s += v[i];
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            int e = lane + 32 * i;
-            v[i] = (e < E) ? v[i] / s : -1.f;   // -1: never selected
-            if (e < E) pacc[i] += v[i];
-        }
-        // top-k (+ the next one for the gap)
-        uint32_t taken = 0;
-        float my_val = 0.f;
-        int my_idx = 0;
-        float kth = 0.f, sel_sum = 0.f;
-        const int rounds = k < E ? k + 1 : k;
-        for (int j = 0; j < rounds; j++) {
-            float bv = -2.f;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                int e = lane + 32 * i;
-                if (!(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                    bv = v[i];
-                    bi = e;
-                }
-            }
-            warp_argmax(bv, bi);
-            if (j < k) {
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-                if (lane == j) {
-                    my_val = bv;
-                    my_idx = bi;
-                }
-                sel_sum += bv;   // slot order, identical on every lane
-                kth = bv;
-            } else if (lane == 0 && gap_out) {
-                gap_out[tok] = kth - bv;
-            }
-        }
-        if (k >= E && lane == 0 && gap_out) gap_out[tok] = __int_as_float(0x7f800000);
-        if (lane < k) {
-            idx_out[tok * k + lane] = my_idx;
-            w_out[tok * k + lane] = renorm ? my_val / sel_sum : my_val;
-        }
+        for (int i = 0; i < NV; i++) v[i] = Ls[t * (EP + 1) + lane + 32 * i];
+        finish_token<NV>(v, b_r, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
     }
-
-    // per-block column sums of the probabilities, combined across warps in warp order
     __syncthreads();             // every warp is done reading the logits
-    float* Pw = sm;              // [warps][EP]
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        int e = lane + 32 * i;
-        if (e < EP) Pw[warp * EP + e] = pacc[i];
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kRouterThreads) {
-        float sacc = 0.f;
-        for (int w = 0; w < kWarps; w++) sacc += Pw[w * EP + e];
-        p_part[(int64_t)blockIdx.x * E + e] = sacc;
-    }
+    write_p_part<NV>(pacc, sm, E, p_part);
 }
 
 __global__ void reduce_p_kernel(const float* __restrict__ p_part, int blocks, int E,
                                 float* __restrict__ P_sum) {
-    int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     float s = 0.f;
     for (int b = 0; b < blocks; b++) s += p_part[(int64_t)b * E + e];
@@ -242,59 +382,85 @@ int pad_experts(int E) {
     return ep;
 }
 
-template <int EP>
-cudaError_t launch_ep(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
-                      int32_t* idx, float* w, float* gap, float* p_part, cudaStream_t s) {
-    using Tl = RouterTile<EP>;
-    int blocks = (int)((c.N + Tl::BT - 1) / Tl::BT);
-    const float* bias = c.bias_mode == 1 ? b_r : nullptr;
-    if (c.act_dtype == MOE_BF16)
-        router_kernel<EP, __nv_bfloat16><<<blocks, kRouterThreads, 0, s>>>(
-            (const __nv_bfloat16*)x, W_r, bias, c.N, c.d, c.E, c.k, c.renorm, idx, w, gap, p_part);
-    else
-        router_kernel<EP, float><<<blocks, kRouterThreads, 0, s>>>(
-            (const float*)x, W_r, bias, c.N, c.d, c.E, c.k, c.renorm, idx, w, gap, p_part);
-    return cudaGetLastError();
+template <typename Kernel, typename T>
+void launch_k(Kernel kern, int blocks, cudaStream_t s, const T* x, const float* W_r,
+              const float* bias, const moe_cfg& c, int32_t* idx, float* w, float* gap,
+              float* p_part) {
+    kern<<<blocks, kRouterThreads, 0, s>>>(x, W_r, bias, c.N, c.d, c.E, c.k, c.renorm, idx, w,
+                                           gap, p_part);
+}
+
+template <int EP, typename T>
+int launch_gemv(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
+                float* w, float* gap, float* p_part, cudaStream_t s) {
+    const int blocks = (int)((c.N + kGemvTokensPerBlock - 1) / kGemvTokensPerBlock);
+    launch_k(router_gemv_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, p_part);
+    return blocks;
+}
+
+template <int EP, typename T>
+int launch_tiled(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
+                 float* w, float* gap, float* p_part, cudaStream_t s) {
+    const int blocks = (int)((c.N + RouterTile<EP>::BT - 1) / RouterTile<EP>::BT);
+    launch_k(router_tiled_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, p_part);
+    return blocks;
+}
+
+template <int NV>
+int launch_topk(const moe_cfg& c, const float* logits, const float* bias, int32_t* idx, float* w,
+                float* gap, float* p_part, cudaStream_t s) {
+    const int blocks = (int)((c.N + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
+    logits_topk_kernel<NV><<<blocks, kRouterThreads, 0, s>>>(logits, bias, c.N, c.E, c.k, c.renorm,
+                                                             idx, w, gap, p_part);
+    return blocks;
+}
+
+template <typename T>
+int dispatch_simt(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
+                  float* w, float* gap, float* p_part, cudaStream_t s) {
+    switch (pad_experts(c.E)) {
+        case 8: return launch_gemv<8>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 16: return launch_gemv<16>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 32: return launch_gemv<32>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 64: return launch_tiled<64>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 128: return launch_tiled<128>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 256: return launch_tiled<256>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        case 512: return launch_tiled<512>(c, x, W_r, bias, idx, w, gap, p_part, s);
+        default: return launch_tiled<1024>(c, x, W_r, bias, idx, w, gap, p_part, s);
+    }
 }
 
 }  // namespace
 
-int router_block_tokens(int E) {
-    switch (pad_experts(E)) {
-        case 8: return RouterTile<8>::BT;
-        case 16: return RouterTile<16>::BT;
-        case 32: return RouterTile<32>::BT;
-        case 64: return RouterTile<64>::BT;
-        case 128: return RouterTile<128>::BT;
-        case 256: return RouterTile<256>::BT;
-        case 512: return RouterTile<512>::BT;
-        default: return RouterTile<1024>::BT;
-    }
-}
+bool router_uses_tensor_cores(const moe_cfg& c) { return c.act_dtype == MOE_BF16 && c.E > 32; }
 
-int router_blocks(int64_t N, int E) {
-    int bt = router_block_tokens(E);
-    return (int)((N + bt - 1) / bt);
-}
+int64_t router_part_rows(int64_t N) { return (N + 7) / 8 + 1; }
 
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* p_part, float* P_sum,
-                          cudaStream_t s) {
-    cudaError_t err = cudaSuccess;
+                          __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s) {
+    const float* bias = c.bias_mode == 1 ? b_r : nullptr;
+    int blocks = 0;
     if (c.N > 0) {
-        switch (pad_experts(c.E)) {
-            case 8: err = launch_ep<8>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 16: err = launch_ep<16>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 32: err = launch_ep<32>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 64: err = launch_ep<64>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 128: err = launch_ep<128>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 256: err = launch_ep<256>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            case 512: err = launch_ep<512>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
-            default: err = launch_ep<1024>(c, x, W_r, b_r, idx, w, gap, p_part, s); break;
+        if (router_uses_tensor_cores(c)) {
+            cudaError_t e = tc_router_logits((const __nv_bfloat16*)x, c.N, c.d, W_r, c.E, w3,
+                                             logits, err, s);
+            if (e != cudaSuccess) return e;
+            switch (pad_experts(c.E) / 32) {
+                case 1: case 2: blocks = launch_topk<2>(c, logits, bias, idx, w, gap, p_part, s); break;
+                case 4: blocks = launch_topk<4>(c, logits, bias, idx, w, gap, p_part, s); break;
+                case 8: blocks = launch_topk<8>(c, logits, bias, idx, w, gap, p_part, s); break;
+                case 16: blocks = launch_topk<16>(c, logits, bias, idx, w, gap, p_part, s); break;
+                default: blocks = launch_topk<32>(c, logits, bias, idx, w, gap, p_part, s); break;
+            }
+        } else if (c.act_dtype == MOE_BF16) {
+            blocks = dispatch_simt(c, (const __nv_bfloat16*)x, W_r, bias, idx, w, gap, p_part, s);
+        } else {
+            blocks = dispatch_simt(c, (const float*)x, W_r, bias, idx, w, gap, p_part, s);
         }
-        if (err != cudaSuccess) return err;
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    int blocks = router_blocks(c.N, c.E);
     reduce_p_kernel<<<(c.E + 255) / 256, 256, 0, s>>>(p_part, blocks, c.E, P_sum);
     return cudaGetLastError();
 }

@@ -1,0 +1,256 @@
+// router_tc.cu -- router logits l = x W_r^T on the tensor cores, still fp32-accurate.
+//
+// Page "混合专家 MoE", section "实现：逐 token 与按专家分组", MoE.route: the router is a linear
+// layer d -> E whose scores decide the top-k.  The router weight is fp32 and x is bf16.  Each
+// fp32 weight w splits exactly into three bf16 numbers, w = hi + mid + lo (hi = bf16(w),
+// mid = bf16(w - hi), lo = w - hi - mid, each subtraction exact), so every product x * part is
+// exact in fp32 and l = x.hi + x.mid + x.lo loses nothing to the split.  The three parts are
+// stacked as the N dimension of one MMA (N = 3 x 64 experts).
+//
+// Accuracy of the sum: TMEM accumulates in fp32 over 256-wide slices of d only; after each
+// slice the epilogue reads the three partial sums, adds them smallest first, and adds the
+// slice into the running logit with compensated (Kahan) summation.  The logit error therefore
+// stays near the error of a 256-term fp32 sum, whatever d is.
+//
+// One CTA = 128 tokens x 64 experts, 320 threads:
+//   warp 0      TMA producer: x tile 128x64 and the hi/mid/lo rows 3 x 64x64 per k-block,
+//               4-stage ring (40 KB per stage, 128-byte swizzle);
+//   warp 1      TMEM allocation (512 columns: two 192-column slice accumulators) and the
+//               single MMA-issuing thread (tcgen05.mma M=128, N=192, K=16);
+//   warps 2..9  two epilogue warpgroups, experts [0,32) and [32,64) of the tile.
+// Logits are written as fp32 [N, E]; softmax and top-k follow in router.cu.
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int RBM = 128;                 // tokens per tile
+constexpr int REN = 64;                  // experts per tile
+constexpr int RN = 3 * REN;              // MMA N: hi | mid | lo
+constexpr int RBK = 64;
+constexpr int RSTAGES = 4;
+constexpr int SLICE_KB = 4;              // k-blocks per TMEM read-out (256 of d)
+constexpr int RA_STAGE = RBM * RBK * 2;  // 16 KB
+constexpr int RB_PART = REN * RBK * 2;   // 8 KB
+constexpr int RB_STAGE = 3 * RB_PART;    // 24 KB
+constexpr int RSTAGE = RA_STAGE + RB_STAGE;
+constexpr int RTHREADS = 320;
+constexpr uint32_t RTMEM_COLS = 512;
+constexpr int RSMEM = RSTAGES * RSTAGE + 1024 + 256;
+
+__global__ void split3_kernel(const float* __restrict__ W, int64_t n, __nv_bfloat16* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float w = W[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        out[i] = hi;
+        out[n + i] = mid;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+}
+
+__global__ void __launch_bounds__(RTHREADS, 1)
+router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                 int64_t N, int d, int E, float* __restrict__ logits, int32_t* err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + RSTAGES * RA_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RSTAGES * RSTAGE);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + RSTAGES;
+    uint64_t* tfull = bars + 2 * RSTAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * RBM;
+    const int e0 = blockIdx.y * REN;
+    const int nk = (d + RBK - 1) / RBK;
+    const int nslices = (nk + SLICE_KB - 1) / SLICE_KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RSTAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 256);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), RTMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int last_ph[RSTAGES];
+            for (int i = 0; i < RSTAGES; i++) last_ph[i] = -1;
+            bool ok = true;
+            for (int kb = 0; kb < nk; kb++) {
+                if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], RSTAGE);
+                const int kx = kb * RBK;
+                tma_load_2d(smem_u32(sA + s * RA_STAGE), &tmX, &full[s], kx, m0);
+#pragma unroll
+                for (int p = 0; p < 3; p++)
+                    tma_load_2d(smem_u32(sB + s * RB_STAGE + p * RB_PART), &tmW, &full[s], kx,
+                                p * E + e0);
+                last_ph[s] = (int)ph;
+                if (++s == RSTAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok)
+                for (int i = 0; i < RSTAGES; i++)
+                    if (last_ph[i] >= 0)
+                        wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(RBM, RN);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int sl = 0; sl < nslices && ok; sl++) {
+                const int acc = sl & 1;
+                const uint32_t aph = (uint32_t)(sl >> 1) & 1u;
+                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+                const int kb_end = min(nk, (sl + 1) * SLICE_KB);
+                for (int kb = sl * SLICE_KB; kb < kb_end; kb++) {
+                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * RA_STAGE);
+                    const uint32_t b0 = smem_u32(sB + s * RB_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < RBK / 16; kk++)
+                        umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                                  (kb > sl * SLICE_KB || kk > 0) ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                    if (++s == RSTAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&tfull[acc]);
+            }
+            umma_commit(drain);
+            wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue: 2 warpgroups x 4 quarters
+        const int q = warp & 3;
+        const int wg = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        float acc[32], cmp[32];
+#pragma unroll
+        for (int j = 0; j < 32; j++) acc[j] = cmp[j] = 0.f;
+        bool ok = true;
+        for (int sl = 0; sl < nslices; sl++) {
+            const int a = sl & 1;
+            const uint32_t aph = (uint32_t)(sl >> 1) & 1u;
+            if (!waitw(&tfull[a], aph, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * 256 + wg * 32);
+            uint32_t p0[32], p1[32], p2[32];
+            tmem_ld32(t, p0);
+            tmem_ld32(t + REN, p1);
+            tmem_ld32(t + 2 * REN, p2);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const float s = (__uint_as_float(p2[j]) + __uint_as_float(p1[j])) +
+                                __uint_as_float(p0[j]);
+                const float y = s - cmp[j];
+                const float tt = acc[j] + y;
+                cmp[j] = (tt - acc[j]) - y;
+                acc[j] = tt;
+            }
+        }
+        const int64_t tok = (int64_t)m0 + row;
+        const int ebase = e0 + wg * 32;
+        if (ok && tok < N) {
+            float* dst = logits + tok * E + ebase;
+            if (ebase + 32 <= E && (E & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; j++)
+                    if (ebase + j < E) dst[j] = acc[j];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, RTMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && err) atomicOr(err, MOE_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
+                             __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
+    const int64_t n = (int64_t)E * d;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    split3_kernel<<<blocks, 256, 0, s>>>(W_r, n, w3);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, N, d, RBM) || !make_map(&mw, w3, 3 * (int64_t)E, d, REN))
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((N + RBM - 1) / RBM), (unsigned)((E + REN - 1) / REN));
+    router_tc_kernel<<<grid, RTHREADS, RSMEM, s>>>(mx, mw, N, d, E, logits, err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
