@@ -151,6 +151,8 @@ def main():
     ap.add_argument("--workload", default=moe_synth.MIXTRAL.name,
                     choices=sorted(moe_synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the batch size N (smaller cases for profiling; not a bench line)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU-oracle budget for the cpu_baseline field (0 to skip)")
     args = ap.parse_args()
@@ -159,6 +161,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     spec = moe_synth.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        spec = spec.with_(N=args.tokens, name=f"{spec.name}_N{args.tokens}")
     peaks, peak_src = load_peaks()
 
     if args.impl == "reference":
@@ -269,7 +273,7 @@ def main():
     if rank == 0:
         line = {
             "metric": "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
-            if spec is moe_synth.MIXTRAL else f"MoE layer forward tokens/s ({spec.name})",
+            if spec == moe_synth.MIXTRAL else f"MoE layer forward tokens/s ({spec.name})",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if act_b == 2 else "f32",
