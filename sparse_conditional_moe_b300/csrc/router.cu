@@ -367,13 +367,18 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
     write_p_part<NV>(pacc, sm, E, p_part);
 }
 
+// P_sum[e] = sum over router blocks of p_part[b][e]: one warp per expert, lanes take every
+// 32nd block, fixed butterfly (deterministic).
 __global__ void reduce_p_kernel(const float* __restrict__ p_part, int blocks, int E,
                                 float* __restrict__ P_sum) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (e >= E) return;
     float s = 0.f;
-    for (int b = 0; b < blocks; b++) s += p_part[(int64_t)b * E + e];
-    P_sum[e] = s;
+    for (int b = lane; b < blocks; b += 32) s += p_part[(int64_t)b * E + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) P_sum[e] = s;
 }
 
 int pad_experts(int E) {
@@ -461,7 +466,7 @@ cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, con
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    reduce_p_kernel<<<(c.E + 255) / 256, 256, 0, s>>>(p_part, blocks, c.E, P_sum);
+    reduce_p_kernel<<<(c.E + 7) / 8, 256, 0, s>>>(p_part, blocks, c.E, P_sum);
     return cudaGetLastError();
 }
 
