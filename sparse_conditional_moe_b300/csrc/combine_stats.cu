@@ -78,7 +78,25 @@ combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T
                 p[j] = v;
             }
         }
-        for (int c = lane; c < chunks; c += 32) {
+        int c = lane;
+        for (; c + 32 < chunks; c += 64) {   // two column chunks per pass: 2(k+S) loads in flight
+            float a[V], b[V];
+#pragma unroll
+            for (int i = 0; i < V; i++) a[i] = b[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (j < k && p[j] >= 0) {
+                    Vec<T>::add(y + (int64_t)p[j] * d + c * V, a);
+                    Vec<T>::add(y + (int64_t)p[j] * d + (c + 32) * V, b);
+                }
+            for (int s = 0; s < S; s++) {
+                Vec<T>::add(ysh + ((int64_t)s * N + t) * d + c * V, a);
+                Vec<T>::add(ysh + ((int64_t)s * N + t) * d + (c + 32) * V, b);
+            }
+            Vec<T>::store(out + t * d + c * V, a);
+            Vec<T>::store(out + t * d + (c + 32) * V, b);
+        }
+        for (; c < chunks; c += 32) {
             float a[V];
 #pragma unroll
             for (int i = 0; i < V; i++) a[i] = 0.f;

@@ -37,7 +37,8 @@ constexpr int B_STAGE = BN * BK * 2;
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+constexpr int STAGING_BYTES = 4 * 2 * 2048;   // epilogue: 4 warps x 2 buffers x 32x32 bf16
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
 enum { EPI_SWIGLU = 0, EPI_SCALE = 1 };
 
@@ -77,8 +78,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int tile) {
         const int per = mtg * p.n_tiles;
         t.g = tile / per;
         const int local = tile - t.g * per;
-        t.mt = local % mtg;
-        t.nt = local / mtg;
+        raster_tile(local, mtg, p.n_tiles, t.mt, t.nt);
         t.rows = p.uniform_rows;
         t.a_row0 = (int64_t)t.g * p.a_stride;
         t.c_row0 = (int64_t)t.g * p.c_stride;
@@ -94,8 +94,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int tile) {
         const int mt0 = p.mtile_off[lo];
         const int mtg = p.mtile_off[lo + 1] - mt0;
         const int local = tile - mt0 * p.n_tiles;
-        t.mt = local % mtg;
-        t.nt = local / mtg;
+        raster_tile(local, mtg, p.n_tiles, t.mt, t.nt);
         t.rows = p.rows[lo];
         t.a_row0 = t.c_row0 = p.row_off[lo];
     }
@@ -114,13 +113,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                  const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+                  const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC,
+                  const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* sStage = smem + STAGES * STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGING_BYTES);
     uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
     uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
     uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
@@ -146,6 +147,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB0);
         if (EPI == EPI_SWIGLU) prefetch_tmap(&tmB1);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -247,6 +249,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ---------------------------------------------------- epilogue (warps 2..5)
         const int q = warp & 3;   // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
+        const uint32_t stage0 = smem_u32(sStage) + (uint32_t)(warp - 2) * 4096u;
+        int nchunk = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -256,61 +260,53 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const TileInfo t = decode_tile(p, tile);
             const int r = t.mt * BM + row_in_tile;
             const bool valid = r < t.rows;
+            const bool all_valid = t.mt * BM + q * 32 + 31 < t.rows;   // warp-uniform
             const int64_t crow = t.c_row0 + r;
+            const int32_t gy = (int32_t)(t.c_row0 + t.mt * BM + q * 32);
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if (EPI == EPI_SWIGLU) {
                 const int col0 = t.nt * (BN / 2);
 #pragma unroll 1
-                for (int c = 0; c < (BN / 2) / 32; c++) {
+                for (int c = 0; c < (BN / 2) / 32; c++, nchunk++) {
                     uint32_t g[32], u[32];
                     tmem_ld32(taddr + c * 32, g);
                     tmem_ld32(taddr + BN / 2 + c * 32, u);
                     tmem_ld_wait();
-                    if (valid) {
-                        uint32_t pk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int j = 0; j < 16; j++) {
-                            float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                            float h1 =
-                                silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-                            pk[j] = pack_bf16(h0, h1);
-                        }
-                        const int col = col0 + c * 32;
-                        __nv_bfloat16* dst = p.C + crow * p.ldc + col;
-#pragma unroll
-                        for (int v = 0; v < 4; v++)
-                            if (col + v * 8 + 8 <= p.n_out)
-                                *reinterpret_cast<uint4*>(dst + v * 8) =
-                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int j = 0; j < 16; j++) {
+                        const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                        const float h1 =
+                            silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                        pk[j] = pack_bf16(h0, h1);
                     }
+                    const int col = col0 + c * 32;
+                    store_chunk32(&tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
+                                  p.C + crow * p.ldc + col, col, p.n_out, gy);
                 }
             } else {
                 const int col0 = t.nt * BN;
                 const float sc = (valid && p.row_scale) ? p.row_scale[crow] : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; c++) {
+                for (int c = 0; c < BN / 32; c++, nchunk++) {
                     uint32_t a[32];
                     tmem_ld32(taddr + c * 32, a);
                     tmem_ld_wait();
-                    if (valid) {
-                        uint32_t pk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int j = 0; j < 16; j++)
-                            pk[j] = pack_bf16(__uint_as_float(a[2 * j]) * sc,
-                                              __uint_as_float(a[2 * j + 1]) * sc);
-                        const int col = col0 + c * 32;
-                        __nv_bfloat16* dst = p.C + crow * p.ldc + col;
-#pragma unroll
-                        for (int v = 0; v < 4; v++)
-                            if (col + v * 8 + 8 <= p.n_out)
-                                *reinterpret_cast<uint4*>(dst + v * 8) =
-                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
+                    for (int j = 0; j < 16; j++)
+                        pk[j] = pack_bf16(__uint_as_float(a[2 * j]) * sc,
+                                          __uint_as_float(a[2 * j + 1]) * sc);
+                    const int col = col0 + c * 32;
+                    store_chunk32(&tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
+                                  p.C + crow * p.ldc + col, col, p.n_out, gy);
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
+        if (lane == 0) bulk_wait_all();   // staged stores done before the CTA can exit
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -348,11 +344,11 @@ int grid_for(const GroupGeom& g, int n_tiles) {
 
 template <int EPI>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                   const TcParams& p, int grid, cudaStream_t s) {
+                   const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    tc_grouped_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+    tc_grouped_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, c, p);
     return cudaGetLastError();
 }
 
@@ -361,11 +357,10 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 cudaError_t tc_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
                       __nv_bfloat16* H, int64_t h_rows, int32_t* err, cudaStream_t s) {
-    (void)h_rows;
     if (g.G <= 0 || a_rows <= 0) return cudaSuccess;
-    CUtensorMap ma, mg, mu;
+    CUtensorMap ma, mg, mu, mc;
     if (!make_map(&ma, A, a_rows, K, BM) || !make_map(&mg, Wg, (int64_t)g.G * F, K, BN / 2) ||
-        !make_map(&mu, Wu, (int64_t)g.G * F, K, BN / 2))
+        !make_map(&mu, Wu, (int64_t)g.G * F, K, BN / 2) || !make_store_map(&mc, H, h_rows, F))
         return cudaErrorInvalidValue;
     TcParams p = base_params(g);
     p.K = K;
@@ -376,16 +371,16 @@ cudaError_t tc_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows
     p.ldc = F;
     p.row_scale = nullptr;
     p.err = err;
-    return launch<EPI_SWIGLU>(ma, mg, mu, p, grid_for(g, p.n_tiles), s);
+    return launch<EPI_SWIGLU>(ma, mg, mu, mc, p, grid_for(g, p.n_tiles), s);
 }
 
 cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
                     const __nv_bfloat16* Wd, int D, const float* row_scale,
                     __nv_bfloat16* Y, int64_t y_rows, int32_t* err, cudaStream_t s) {
-    (void)y_rows;
     if (g.G <= 0 || h_rows <= 0) return cudaSuccess;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, H, h_rows, F, BM) || !make_map(&mb, Wd, (int64_t)g.G * D, F, BN))
+    CUtensorMap ma, mb, mc;
+    if (!make_map(&ma, H, h_rows, F, BM) || !make_map(&mb, Wd, (int64_t)g.G * D, F, BN) ||
+        !make_store_map(&mc, Y, y_rows, D))
         return cudaErrorInvalidValue;
     TcParams p = base_params(g);
     p.K = F;
@@ -396,7 +391,7 @@ cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, 
     p.ldc = D;
     p.row_scale = row_scale;
     p.err = err;
-    return launch<EPI_SCALE>(ma, mb, mb, p, grid_for(g, p.n_tiles), s);
+    return launch<EPI_SCALE>(ma, mb, mb, mc, p, grid_for(g, p.n_tiles), s);
 }
 
 }  // namespace moe

@@ -1,6 +1,7 @@
 // moe_api.cu -- the C ABI of libmoe.so: argument validation, workspace layout and the order of
 // launches for each entry point declared in include/moe.h.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "moe_internal.cuh"
@@ -18,6 +19,19 @@ int device_sm_count() {
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+// Groups of >= 512 rows on average run on CTA pairs: a pair always takes two 128-row m-tiles of
+// one group, so the masked half of an odd group's last pair costs little next to the lighter
+// per-SM operand traffic.  MOE_TC_PAIRS=0/1 forces the choice (tuning only).
+bool use_cta_pairs(int64_t avg_rows) {
+    static int forced = -2;
+    if (forced == -2) {
+        const char* e = getenv("MOE_TC_PAIRS");
+        forced = e ? (atoi(e) != 0) : -1;
+    }
+    if (forced >= 0) return forced == 1;
+    return avg_rows >= 512;
 }
 
 int64_t capacity(const moe_cfg& c) {
@@ -141,7 +155,9 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     int32_t* mtile = at<int32_t>(ws, L.mtile_off);
     const int64_t R = grouped_rows(*c);
     const bool bf16 = c->act_dtype == MOE_BF16;
-    MOE_CUDA(launch_plan_mtiles(kept, c->E, bf16 ? kTcBlockRows : simt_block_rows(), mtile, s));
+    const bool pairs = bf16 && use_cta_pairs(R / c->E);
+    const int bm = !bf16 ? simt_block_rows() : (pairs ? 2 * kTcBlockRows : kTcBlockRows);
+    MOE_CUDA(launch_plan_mtiles(kept, c->E, bm, mtile, s));
     GroupGeom g{};
     g.G = c->E;
     g.rows = kept;
@@ -149,7 +165,10 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     g.mtile_off = mtile;
     g.max_rows = R;
     void* h = at<void>(ws, L.h_perm);
-    if (bf16) {
+    if (pairs) {
+        MOE_CUDA(tc2_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
+                            (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, err, s));
+    } else if (bf16) {
         MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
                            (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
     } else {
@@ -157,7 +176,10 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
                                  (const float*)Wu, c->d_ff, (float*)h, s));
     }
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
-    if (bf16) {
+    if (pairs) {
+        MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
+                          row_weight, (__nv_bfloat16*)y_perm, err, s));
+    } else if (bf16) {
         MOE_CUDA(tc_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
                          row_weight, (__nv_bfloat16*)y_perm, R, err, s));
     } else {
@@ -181,7 +203,15 @@ moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int
         g.G = S;
         g.uniform_rows = (int)c->N;
         g.max_rows = c->N;
-        if (c->act_dtype == MOE_BF16) {
+        if (c->act_dtype == MOE_BF16 && use_cta_pairs(c->N)) {
+            g.a_stride = 0;        // every shared expert reads all tokens of x
+            g.c_stride = c->N;
+            MOE_CUDA(tc2_gateup(g, (const __nv_bfloat16*)x, c->N, c->d, (const __nv_bfloat16*)Wsg,
+                                (const __nv_bfloat16*)Wsu, Fs, (__nv_bfloat16*)hsh, err, s));
+            g.a_stride = c->N;
+            MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)hsh, S * c->N, Fs, (const __nv_bfloat16*)Wsd,
+                              c->d, nullptr, (__nv_bfloat16*)ysh, err, s));
+        } else if (c->act_dtype == MOE_BF16) {
             g.a_stride = 0;        // every shared expert reads all tokens of x
             g.c_stride = c->N;
             MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x, c->N, c->d, (const __nv_bfloat16*)Wsg,

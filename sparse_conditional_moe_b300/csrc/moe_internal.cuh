@@ -89,6 +89,17 @@ cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, 
                     const __nv_bfloat16* Wd, int D, const float* row_scale,
                     __nv_bfloat16* Y, int64_t y_rows, int32_t* err, cudaStream_t s);
 
+// The same two GEMMs on CTA pairs (tcgen05 cta_group::2, 256-row m-pairs; GroupGeom.mtile_off
+// then holds m-pair offsets).
+cudaError_t tc2_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
+                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
+                       __nv_bfloat16* H, int32_t* err, cudaStream_t s);
+cudaError_t tc2_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
+                     const __nv_bfloat16* Wd, int D, const float* row_scale, __nv_bfloat16* Y,
+                     int32_t* err, cudaStream_t s);
+// Whether groups of about `avg_rows` rows run on CTA pairs (see moe_api.cu).
+bool use_cta_pairs(int64_t avg_rows);
+
 // fp32 CUDA-core grouped GEMMs (fp32 layers); their m-tiles are simt_block_rows() tall
 int simt_block_rows();
 cudaError_t simt_gateup_f32(const GroupGeom& g, const float* A, int K, const float* Wg,

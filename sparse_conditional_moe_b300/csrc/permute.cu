@@ -202,7 +202,16 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_
         }
         const uint4* src = x + t * row_vecs;
         uint4* dst = xp + r * row_vecs;
-        for (int v = lane; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+        int v = lane;
+        for (; v + 96 < row_vecs; v += 128) {   // four 16-byte loads in flight per lane
+            const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
+                        e = __ldg(src + v + 96);
+            dst[v] = a;
+            dst[v + 32] = b;
+            dst[v + 64] = c;
+            dst[v + 96] = e;
+        }
+        for (; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
     }
 }
 

@@ -107,6 +107,189 @@ static __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- TMA stores
+
+// Shared -> global tile store, tracked by the issuing thread's bulk groups.
+static __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                                    int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+// L2 eviction policies for cache hints.
+static __device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+static __device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+static __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src,
+                                                         int32_t c0, int32_t c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::
+            "l"(reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(src), "l"(policy)
+        : "memory");
+}
+static __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map,
+                                                        uint64_t* bar, int32_t c0, int32_t c1,
+                                                        uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+static __device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+static __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+static __device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+static __device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+static __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                    uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// One epilogue warp writes its 32 rows x 32 bf16 columns (lane = row, pk = the row's 16 packed
+// pairs).  A chunk whose 32 rows all belong to the group goes through the warp's 2 KB staging
+// buffer (64-byte rows, 64-byte swizzle: conflict-free 16-byte stores) and one TMA store of
+// whole lines; a chunk that crosses the end of the group is written row by row for its valid
+// rows only, so rows of the next group are never touched.  Columns past n_out are clipped (TMA)
+// or skipped (direct).  The warp alternates between two buffers; the TMA store that used a
+// buffer two chunks ago must have finished reading it.
+static __device__ __forceinline__ void store_chunk32(const CUtensorMap* tmC, uint32_t buf,
+                                                     const uint32_t (&pk)[16], bool all_valid,
+                                                     bool valid, __nv_bfloat16* dst, int col,
+                                                     int n_out, int32_t gy) {
+    const int lane = threadIdx.x & 31;
+    if (all_valid) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t rowb = buf + (uint32_t)lane * 64u;
+        const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+        for (int v = 0; v < 4; v++)
+            st_shared_v4(rowb + (((uint32_t)v ^ sw) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                         pk[4 * v + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {   // the output is read once, later: keep it from evicting operands
+            tma_store_2d_hint(tmC, buf, col, gy, policy_evict_first());
+            bulk_commit();
+        }
+    } else if (valid) {
+#pragma unroll
+        for (int v = 0; v < 4; v++)
+            if (col + v * 8 + 8 <= n_out)
+                *reinterpret_cast<uint4*>(dst + v * 8) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+}
+
+// ---------------------------------------------------------------- tile order inside a group
+
+// Tile `local` of a group with mtg m-tiles and nt n-tiles -> (m-tile, n-tile).  m-tiles run in
+// blocks of kMBlock: inside a block the m-tiles are innermost (CTAs working together share one
+// weight tile through L2) and the block's n-tiles come one after another, so an A panel of
+// kMBlock m-tiles stays in L2 while all n-tiles sweep it.  Groups with at most kMBlock m-tiles
+// keep the plain m-innermost order.
+constexpr int kMBlock = 16;
+static __device__ __forceinline__ void raster_tile(int local, int mtg, int ntiles, int& mt, int& nt) {
+    const int full = mtg / kMBlock;
+    const int per_block = kMBlock * ntiles;
+    const int mb = local / per_block;
+    if (mb < full) {
+        const int w = local - mb * per_block;
+        nt = w / kMBlock;
+        mt = mb * kMBlock + w % kMBlock;
+    } else {
+        const int rem = mtg - full * kMBlock;
+        const int w = local - full * per_block;
+        nt = w / rem;
+        mt = full * kMBlock + w % rem;
+    }
+}
+
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+
+static __device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of this cluster
+static __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+static __device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
+static __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an mbarrier that may
+// live in the peer CTA (the pair's leader); bar_cluster is a shared::cluster address.
+static __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                        uint32_t bar_cluster, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+static __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+static __device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+static __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D (M=256 over the pair) (+)= A (each CTA its 128 rows) * B (each CTA half of N)^T.
+static __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                      uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at this offset in every CTA of cta_mask once the pair's MMAs issued so
+// far by this thread have completed.
+static __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
 // 8-row core-matrix groups 1024 bytes apart (stride byte offset), tile base 1024-aligned.
 static __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -194,6 +377,19 @@ inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 map for epilogue stores: box = 32 rows x 32 columns (64-byte rows, 64-byte swizzle).
+inline bool make_store_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows <= 0 || cols <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc
