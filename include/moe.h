@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned pointer, k > E ... */
-    MOE_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. bias_mode 2, E > 1024) */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid but not implemented (E > 1024, k > 16, ...) */
     MOE_ERR_CUDA = 3,           /* a CUDA runtime call failed */
     MOE_ERR_DEVICE_BOUNDS = 4,  /* device saw an expert index outside [0, E) */
     MOE_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out */
@@ -71,7 +71,10 @@ typedef struct {
     int32_t d_ff_shared;      /* shared expert hidden dim F_s (ignored when S = 0) */
     double capacity_factor;   /* <= 0: no capacity limit; else C = ceil(CF * N * k / E) in fp64 */
     int32_t renorm;           /* 1: renormalise the k weights to sum to 1 (the pages' form) */
-    int32_t bias_mode;        /* 0: no router bias; 1: b_r added to the logits before softmax */
+    int32_t bias_mode;        /* 0: no router bias; 1: b_r added to the logits before softmax;
+                                 2: b_r added to the probabilities for the top-k choice only
+                                 (weights and P stay unbiased: the DeepSeek-V3 balancing bias,
+                                 "混合专家 MoE" 负载均衡 section) */
     int32_t act_dtype;        /* moe_dtype */
 } moe_cfg;
 
@@ -100,10 +103,11 @@ MOE_API int64_t moe_grouped_rows(const moe_cfg *cfg);
  * moe_route -- router ("混合专家 MoE", 实现 section, MoE.route): logits l = x W_r^T (+ b_r),
  * probabilities p = softmax(l) over all E experts (fp32), the k largest p per token in
  * descending order (ties to the lower expert index), and w = p_sel / sum(p_sel).
- *   x [N,d] act dtype; W_r [E,d] fp32; b_r [E] fp32 (used when bias_mode == 1, else ignored)
+ *   x [N,d] act dtype; W_r [E,d] fp32; b_r [E] fp32 (used when bias_mode != 0, else ignored)
  *   idx [N,k] int32 out; w [N,k] fp32 out;
  *   P_sum [E] fp32 out: sum over tokens of p[t,e] (the load-balance P_e times N);
- *   gap [N] fp32 out, nullable: p_(k) - p_(k+1) (+inf when k == E).
+ *   gap [N] fp32 out, nullable: s_(k) - s_(k+1) of the selection scores s (= p, or p + b_r
+ *   with bias_mode 2; +inf when k == E).
  */
 MOE_API moe_status moe_route(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
                      int32_t *idx, float *w, float *P_sum, float *gap,
@@ -243,6 +247,16 @@ MOE_API moe_status moe_stats(const moe_cfg *cfg, const int32_t *counts, const in
                      const float *P_sum, const int32_t *pos, const float *gap,
                      float *f_host, float *P_host, moe_stats_summary *summary_host,
                      void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_selftest_wait_timeout -- failure-path check of the device-side bounded waits (the pages
+ * have no counterpart): launches one block that waits, with the same bounded mbarrier waits as
+ * the tensor-core kernels (single-thread and warp-wide forms), on a barrier nothing completes;
+ * both give up after timeout_us (1 .. 2,000,000) and set MOE_DEVERR_TIMEOUT in the workspace
+ * error word.  The context stays usable.  Asynchronous; read the result with moe_device_error.
+ */
+MOE_API moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint32_t timeout_us,
+                                             void *stream);
 
 /* Synchronises the stream and reads the sticky device error word (MOE_DEVERR_* bits). */
 MOE_API moe_status moe_device_error(void *ws, size_t ws_bytes, int32_t *code_host, void *stream);

@@ -41,6 +41,7 @@ class LayerSpec:
     dtype: str = BF16
     zipf_bias: float = 0.0         # > 0: router bias ln Zipf(s) over expert rank
     renorm: int = 1
+    bias_mode: int = 1             # how a router bias enters: 1 logits, 2 top-k choice only
 
     def with_(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)

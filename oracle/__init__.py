@@ -46,7 +46,7 @@ def lib():
         P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
         L.oracle_round_bf16.argtypes = [D]
         L.oracle_round_bf16.restype = ctypes.c_uint16
-        L.oracle_route.argtypes = [I64, I32, I32, I32, I32, P, P, P, I32, P, P, P, P]
+        L.oracle_route.argtypes = [I64, I32, I32, I32, I32, P, P, P, I32, I32, P, P, P, P]
         L.oracle_capacity.argtypes = [I64, I32, I32, D]
         L.oracle_capacity.restype = I64
         L.oracle_permute.argtypes = [I64, I32, I32, P, I64, P, P, P, P, P, P]
@@ -55,9 +55,9 @@ def lib():
         L.oracle_moe_token.argtypes = [I32, I32, I32, I32, I32, I32, I32, P, P, P,
                                        P, P, P, P, P, P, P]
         L.oracle_forward_naive.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
-                                           P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
+                                           P, P, P, I32, P, P, P, P, P, P, P, P, P, P, P, P]
         L.oracle_forward_grouped.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
-                                             P, P, P, P, P, P, P, P, P, P]
+                                             P, P, P, I32, P, P, P, P, P, P, P]
         L.oracle_stats.argtypes = [I64, I32, I32, P, P, P, P, D, P, P, P, P]
         for fn in ("oracle_route", "oracle_permute", "oracle_moe_token", "oracle_forward_naive",
                    "oracle_forward_grouped", "oracle_stats"):
@@ -103,8 +103,11 @@ def capacity(N: int, k: int, E: int, cf: float) -> int:
 
 # ---------------------------------------------------------------- steps
 
-def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1):
-    """Router: returns idx [N,k] int32, w [N,k] f32, probs [N,E] f32, gap [N] f32."""
+def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1, bias_mode: Optional[int] = None):
+    """Router: returns idx [N,k] int32, w [N,k] f32, probs [N,E] f32, gap [N] f32.
+    bias_mode: 1 = b_r added to the logits (default when b_r is given), 2 = b_r added to the
+    probabilities for the top-k choice only."""
+    bias_mode = (0 if b_r is None else 1) if bias_mode is None else bias_mode
     x = as_host(x, dtype)
     W_r = np.ascontiguousarray(as_host(W_r, F32), dtype=np.float32)
     b = None if b_r is None else np.ascontiguousarray(as_host(b_r, F32), dtype=np.float32)
@@ -114,7 +117,7 @@ def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1):
     w = np.zeros((N, k), np.float32)
     probs = np.zeros((N, E), np.float32)
     gap = np.zeros((N,), np.float32)
-    rc = lib().oracle_route(N, d, E, k, dtype, _p(x), _p(W_r), _p(b), renorm,
+    rc = lib().oracle_route(N, d, E, k, dtype, _p(x), _p(W_r), _p(b), bias_mode, renorm,
                             _p(idx), _p(w), _p(probs), _p(gap))
     if rc:
         raise ValueError("oracle_route rejected its arguments")
@@ -187,9 +190,10 @@ def _layer_arrays(layer, dtype):
 
 
 def forward_naive(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int = 1,
-                  round_h: Optional[int] = None):
+                  round_h: Optional[int] = None, bias_mode: Optional[int] = None):
     """The whole layer token by token.  Returns (out, extras dict)."""
     x, W_r, b_r, Wg, Wu, Wd, Wsg, Wsu, Wsd = _layer_arrays(layer, dtype)
+    bias_mode = (0 if b_r is None else 1) if bias_mode is None else bias_mode
     round_h = (1 if dtype == BF16 else 0) if round_h is None else round_h
     N, d = x.shape
     E, F = Wg.shape[0], Wg.shape[1]
@@ -202,7 +206,7 @@ def forward_naive(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int 
     probs = np.zeros((N, E), np.float32)
     gap = np.zeros((N,), np.float32)
     rc = lib().oracle_forward_naive(N, d, F, E, k, S, Fs, dtype, float(cf), renorm, round_h,
-                                    _p(x), _p(W_r), _p(b_r), _p(Wg), _p(Wu), _p(Wd),
+                                    _p(x), _p(W_r), _p(b_r), bias_mode, _p(Wg), _p(Wu), _p(Wd),
                                     _p(Wsg), _p(Wsu), _p(Wsd), _p(out), _p(idx), _p(w),
                                     _p(keep), _p(probs), _p(gap))
     if rc:
@@ -211,8 +215,9 @@ def forward_naive(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int 
 
 
 def forward_grouped(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int = 1,
-                    round_h: Optional[int] = None):
+                    round_h: Optional[int] = None, bias_mode: Optional[int] = None):
     x, W_r, b_r, Wg, Wu, Wd, Wsg, Wsu, Wsd = _layer_arrays(layer, dtype)
+    bias_mode = (0 if b_r is None else 1) if bias_mode is None else bias_mode
     round_h = (1 if dtype == BF16 else 0) if round_h is None else round_h
     N, d = x.shape
     E, F = Wg.shape[0], Wg.shape[1]
@@ -220,7 +225,7 @@ def forward_grouped(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: in
     Fs = 0 if Wsg is None else Wsg.shape[1]
     out = np.zeros_like(x)
     rc = lib().oracle_forward_grouped(N, d, F, E, k, S, Fs, dtype, float(cf), renorm, round_h,
-                                      _p(x), _p(W_r), _p(b_r), _p(Wg), _p(Wu), _p(Wd),
+                                      _p(x), _p(W_r), _p(b_r), bias_mode, _p(Wg), _p(Wu), _p(Wd),
                                       _p(Wsg), _p(Wsu), _p(Wsd), _p(out))
     if rc:
         raise ValueError("oracle_forward_grouped rejected its arguments")

@@ -93,15 +93,17 @@ static double elem(const void *p, int dtype, int64_t i)
 
 /* For one token: probs[E] (fp32), idx[k], w[k], gap.  Returns 0. */
 static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t,
-                        const float *W_r, const float *b_r, int renorm,
+                        const float *W_r, const float *b_r, int bias_mode, int renorm,
                         float *probs, int32_t *idx, float *w, float *gap)
 {
     float *logit = (float *)malloc(sizeof(float) * (size_t)E);
+    float *sel = (float *)malloc(sizeof(float) * (size_t)E);
     unsigned char *chosen = (unsigned char *)calloc((size_t)E, 1);
 
-    /* logits: l[e] = b_e + sum_i x[t,i] * W_r[e,i], rounded once to fp32 */
+    /* logits: l[e] = (b_e if the bias enters the logits) + sum_i x[t,i] * W_r[e,i],
+     * rounded once to fp32 */
     for (int e = 0; e < E; e++) {
-        double acc = b_r ? (double)b_r[e] : 0.0;
+        double acc = (b_r && bias_mode == 1) ? (double)b_r[e] : 0.0;
         for (int i = 0; i < d; i++)
             acc += elem(x, dtype, t * (int64_t)d + i) * (double)W_r[(int64_t)e * d + i];
         logit[e] = (float)acc;
@@ -118,23 +120,29 @@ static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t
     for (int e = 0; e < E; e++)
         probs[e] = (float)(exp((double)logit[e] - mx) / s);
 
-    /* top-k: k rounds of "largest not yet chosen", ties to the lower index */
+    /* selection score: the probability, or with a selection-only bias ("混合专家 MoE",
+     * 负载均衡: the bias only picks the top-k, it does not change the weights) p_e + b_e,
+     * rounded once to fp32 */
+    for (int e = 0; e < E; e++)
+        sel[e] = (b_r && bias_mode == 2) ? (float)((double)probs[e] + (double)b_r[e]) : probs[e];
+
+    /* top-k: k rounds of "largest score not yet chosen", ties to the lower index */
     for (int j = 0; j < k; j++) {
         int best = -1;
         for (int e = 0; e < E; e++)
-            if (!chosen[e] && (best < 0 || probs[e] > probs[best]))
+            if (!chosen[e] && (best < 0 || sel[e] > sel[best]))
                 best = e;
         idx[j] = best;
         chosen[best] = 1;
     }
 
-    /* gap between the k-th and the (k+1)-th probability (none when k == E) */
+    /* gap between the k-th and the (k+1)-th score (none when k == E) */
     if (k < E) {
         int nb = -1;
         for (int e = 0; e < E; e++)
-            if (!chosen[e] && (nb < 0 || probs[e] > probs[nb]))
+            if (!chosen[e] && (nb < 0 || sel[e] > sel[nb]))
                 nb = e;
-        *gap = (float)((double)probs[idx[k - 1]] - (double)probs[nb]);
+        *gap = (float)((double)sel[idx[k - 1]] - (double)sel[nb]);
     } else {
         *gap = INFINITY;
     }
@@ -147,16 +155,19 @@ static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t
         w[j] = renorm ? (float)((double)probs[idx[j]] / ws) : probs[idx[j]];
 
     free(logit);
+    free(sel);
     free(chosen);
 }
 
 /*
  * oracle_route: router for all N tokens.
- *   x [N,d] (fp32 or bf16 bits), W_r [E,d] fp32, b_r [E] fp32 or NULL.
+ *   x [N,d] (fp32 or bf16 bits), W_r [E,d] fp32, b_r [E] fp32 or NULL;
+ *   bias_mode 1: b_r is added to the logits; 2: b_r is added to the probabilities for the
+ *   top-k choice only (the weights and probs stay unbiased).
  *   idx [N,k] int32, w [N,k] fp32; probs [N,E] fp32 and gap [N] fp32 may be NULL.
  */
 int oracle_route(int64_t N, int d, int E, int k, int dtype, const void *x,
-                 const float *W_r, const float *b_r, int renorm,
+                 const float *W_r, const float *b_r, int bias_mode, int renorm,
                  int32_t *idx, float *w, float *probs, float *gap)
 {
     if (N < 0 || d <= 0 || E <= 0 || k <= 0 || k > E)
@@ -165,7 +176,7 @@ int oracle_route(int64_t N, int d, int E, int k, int dtype, const void *x,
     for (int64_t t = 0; t < N; t++) {
         float *p = (float *)malloc(sizeof(float) * (size_t)E);
         float g;
-        route_token(d, E, k, dtype, x, t, W_r, b_r, renorm, p, idx + t * k, w + t * k, &g);
+        route_token(d, E, k, dtype, x, t, W_r, b_r, bias_mode, renorm, p, idx + t * k, w + t * k, &g);
         if (probs)
             memcpy(probs + t * (int64_t)E, p, sizeof(float) * (size_t)E);
         if (gap)
@@ -337,7 +348,7 @@ void oracle_keep_naive(int64_t N, int k, int E, const int32_t *idx, int64_t capa
  */
 int oracle_forward_naive(int64_t N, int d, int F, int E, int k, int S, int Fs, int dtype,
                          double cf, int renorm, int round_h,
-                         const void *x, const float *W_r, const float *b_r,
+                         const void *x, const float *W_r, const float *b_r, int bias_mode,
                          const void *Wg, const void *Wu, const void *Wd,
                          const void *Wsg, const void *Wsu, const void *Wsd,
                          void *out, int32_t *idx_o, float *w_o, int32_t *keep_o,
@@ -349,7 +360,7 @@ int oracle_forward_naive(int64_t N, int d, int F, int E, int k, int S, int Fs, i
     int32_t *idx = idx_o ? idx_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
     float *w = w_o ? w_o : (float *)malloc(sizeof(float) * (size_t)(A ? A : 1));
     int32_t *keep = keep_o ? keep_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
-    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, renorm, idx, w, probs_o, gap_o);
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, probs_o, gap_o);
     if (rc) {
         if (!idx_o) free(idx);
         if (!w_o) free(w);
@@ -391,7 +402,7 @@ int oracle_forward_naive(int64_t N, int d, int F, int E, int k, int S, int Fs, i
  */
 int oracle_forward_grouped(int64_t N, int d, int F, int E, int k, int S, int Fs, int dtype,
                            double cf, int renorm, int round_h,
-                           const void *x, const float *W_r, const float *b_r,
+                           const void *x, const float *W_r, const float *b_r, int bias_mode,
                            const void *Wg, const void *Wu, const void *Wd,
                            const void *Wsg, const void *Wsu, const void *Wsd, void *out)
 {
@@ -410,7 +421,7 @@ int oracle_forward_grouped(int64_t N, int d, int F, int E, int k, int S, int Fs,
     double *acc = (double *)calloc((size_t)(N * d ? N * d : 1), sizeof(double));
     double *xt = (double *)malloc(sizeof(double) * (size_t)d);
     double *y = (double *)malloc(sizeof(double) * (size_t)d);
-    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, renorm, idx, w, NULL, NULL);
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, NULL, NULL);
     if (!rc)
         rc = oracle_permute(N, k, E, idx, oracle_capacity(N, k, E, cf), counts, offsets, kept,
                             kept_off, perm, pos);

@@ -21,17 +21,17 @@ int device_sm_count() {
     return cached[dev];
 }
 
-// Groups of >= 512 rows on average run on CTA pairs: a pair always takes two 128-row m-tiles of
-// one group, so the masked half of an odd group's last pair costs little next to the lighter
-// per-SM operand traffic.  MOE_TC_PAIRS=0/1 forces the choice (tuning only).
+// CTA pairs (cta_group::2) are opt-in with MOE_TC_PAIRS=1, for groups averaging >= 512 rows.
+// Measured on B300: 1577 vs 1473 TFLOP/s on eight equal 1024-row groups, but on routed layers,
+// whose group sizes straddle multiples of 256, the single-CTA kernel is as fast or faster, so it
+// is the default.
 bool use_cta_pairs(int64_t avg_rows) {
-    static int forced = -2;
-    if (forced == -2) {
+    static int enabled = -1;
+    if (enabled < 0) {
         const char* e = getenv("MOE_TC_PAIRS");
-        forced = e ? (atoi(e) != 0) : -1;
+        enabled = (e && atoi(e) != 0) ? 1 : 0;
     }
-    if (forced >= 0) return forced == 1;
-    return avg_rows >= 512;
+    return enabled == 1 && avg_rows >= 512;
 }
 
 int64_t capacity(const moe_cfg& c) {
@@ -68,6 +68,7 @@ WsLayout ws_layout(const moe_cfg& c) {
     L.blk_hist = take(4 * (size_t)perm_blocks(A) * E);
     L.blk_base = take(4 * (size_t)perm_blocks(A) * E);
     L.mtile_off = take(4 * (size_t)(E + 1));
+    L.tail_plan = take(4 * (size_t)(3 * E + 1));
     L.stats_f = take(4 * (size_t)(2 * E + 8));
     L.idx = take(4 * (size_t)A);
     L.w = take(4 * (size_t)A);
@@ -117,7 +118,6 @@ moe_status check_cfg(const moe_cfg* c) {
         return MOE_ERR_INVALID_ARG;
     if (isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (c->E > 1024 || c->k > 16 || c->n_shared > 8) return MOE_ERR_UNSUPPORTED;
-    if (c->bias_mode == 2) return MOE_ERR_UNSUPPORTED;
     if (c->N * (int64_t)c->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     if (grouped_rows(*c) * (int64_t)(c->d > c->d_ff ? c->d : c->d_ff) >= ((int64_t)1 << 40))
         return MOE_ERR_UNSUPPORTED;
@@ -156,18 +156,31 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     const int64_t R = grouped_rows(*c);
     const bool bf16 = c->act_dtype == MOE_BF16;
     const bool pairs = bf16 && use_cta_pairs(R / c->E);
-    const int bm = !bf16 ? simt_block_rows() : (pairs ? 2 * kTcBlockRows : kTcBlockRows);
-    MOE_CUDA(launch_plan_mtiles(kept, c->E, bm, mtile, s));
     GroupGeom g{};
     g.G = c->E;
     g.rows = kept;
     g.row_off = kept_offsets;
     g.mtile_off = mtile;
     g.max_rows = R;
+    GroupGeom tail{};   // pair mode: the odd 128-row m-tile of each group, on the single-CTA kernel
+    if (pairs) {
+        int32_t* tp = at<int32_t>(ws, L.tail_plan);
+        MOE_CUDA(launch_plan_pairs(kept, kept_offsets, c->E, mtile, tp, tp + c->E + 1,
+                                   tp + 2 * c->E + 1, s));
+        tail.G = c->E;
+        tail.mtile_off = tp;
+        tail.rows = tp + c->E + 1;
+        tail.row_off = tp + 2 * c->E + 1;
+        tail.max_rows = (int64_t)c->E * kTcBlockRows;
+    } else {
+        MOE_CUDA(launch_plan_mtiles(kept, c->E, bf16 ? kTcBlockRows : simt_block_rows(), mtile, s));
+    }
     void* h = at<void>(ws, L.h_perm);
     if (pairs) {
         MOE_CUDA(tc2_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
                             (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, err, s));
+        MOE_CUDA(tc_gateup(tail, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
+                           (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
     } else if (bf16) {
         MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
                            (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
@@ -179,6 +192,8 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     if (pairs) {
         MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
                           row_weight, (__nv_bfloat16*)y_perm, err, s));
+        MOE_CUDA(tc_down(tail, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
+                         row_weight, (__nv_bfloat16*)y_perm, R, err, s));
     } else if (bf16) {
         MOE_CUDA(tc_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
                          row_weight, (__nv_bfloat16*)y_perm, R, err, s));
@@ -301,7 +316,7 @@ moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const 
     }
     MOE_TRY(need(W_r, 16));
     MOE_TRY(need(P_sum, 4));
-    if (cfg->bias_mode == 1) MOE_TRY(need(b_r, 4));
+    if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
     const WsLayout L = ws_layout(*cfg);
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.p_part), P_sum,
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits),
@@ -379,7 +394,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(need(W_r, 16));
-    if (cfg->bias_mode == 1) MOE_TRY(need(b_r, 4));
+    if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
     MOE_TRY(check_weights(cfg, W_gate, W_up, W_down));
     MOE_TRY(check_shared(cfg, Ws_gate, Ws_up, Ws_down));
     if (cfg->N > 0) {

@@ -33,7 +33,8 @@ struct WsLayout {
     size_t logits;       // float [N, E] (tensor-core router)
     size_t blk_hist;     // int32 [perm_blocks * E]
     size_t blk_base;     // int32 [perm_blocks * E]
-    size_t mtile_off;    // int32 [E + 1]: m-tile prefix of the routed grouped GEMMs
+    size_t mtile_off;    // int32 [E + 1]: m-tile (or m-pair) prefix of the routed grouped GEMMs
+    size_t tail_plan;    // int32 [3E + 1]: tail m-tile prefix, tail rows, tail row offsets
     size_t stats_f;      // float [2E + 8]: f, P, scalars
     size_t idx, w, gap, P_sum, counts, offsets, kept, kept_offsets, perm, pos;
     size_t row_token, row_weight;
@@ -99,6 +100,11 @@ cudaError_t tc2_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows,
                      int32_t* err, cudaStream_t s);
 // Whether groups of about `avg_rows` rows run on CTA pairs (see moe_api.cu).
 bool use_cta_pairs(int64_t avg_rows);
+// Pair/tail split of the routed groups: pair_off [E+1] prefix of full 256-row pairs;
+// tail_mtile [E+1] prefix of tail m-tiles (0 or 1 per group); tail_rows/tail_off [E].
+cudaError_t launch_plan_pairs(const int32_t* kept, const int32_t* kept_off, int E,
+                              int32_t* pair_off, int32_t* tail_mtile, int32_t* tail_rows,
+                              int32_t* tail_off, cudaStream_t s);
 
 // fp32 CUDA-core grouped GEMMs (fp32 layers); their m-tiles are simt_block_rows() tall
 int simt_block_rows();

@@ -48,9 +48,12 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 // Softmax, top-k, gap and renormalisation of one token held by one warp.  v[i] is the logit of
 // expert lane + 32 i (ignored for experts >= E).  Adds the probabilities into pacc.
+// bias_mode 1: b_r is added to the logits; 2: the top-k is chosen on p + b_r (rounded once to
+// fp32) while the weights and probabilities stay unbiased ("混合专家 MoE", 负载均衡: the
+// DeepSeek-V3 bias only picks the experts).
 template <int NV>
-__device__ __forceinline__ void finish_token(float (&v)[NV], const float* __restrict__ b_r, int E,
-                                             int k, int renorm, int64_t tok,
+__device__ __forceinline__ void finish_token(float (&v)[NV], const float* __restrict__ b_r,
+                                             int bias_mode, int E, int k, int renorm, int64_t tok,
                                              int32_t* __restrict__ idx_out,
                                              float* __restrict__ w_out,
                                              float* __restrict__ gap_out, float (&pacc)[NV]) {
@@ -60,7 +63,7 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
     for (int i = 0; i < NV; i++) {
         const int e = lane + 32 * i;
         if (e < E) {
-            if (b_r) v[i] += b_r[e];
+            if (bias_mode == 1) v[i] += b_r[e];
             m = fmaxf(m, v[i]);
         }
     }
@@ -81,29 +84,42 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
         v[i] = (e < E) ? v[i] / s : -1.f;   // -1: never selected
         if (e < E) pacc[i] += v[i];
     }
+    // selection scores: the probabilities, or p + b for the selection-only bias
+    float sv[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        sv[i] = (bias_mode == 2 && e < E) ? v[i] + b_r[e] : v[i];
+    }
     uint32_t taken = 0;
     float my_val = 0.f, kth = 0.f, sel_sum = 0.f;
     int my_idx = 0;
     const int rounds = k < E ? k + 1 : k;
     for (int j = 0; j < rounds; j++) {
-        float bv = -2.f;
+        float bv = -FLT_MAX;
         int bi = INT_MAX;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int e = lane + 32 * i;
-            if (!(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
+            if (e < E && !(taken & (1u << i)) && (sv[i] > bv || (sv[i] == bv && e < bi))) {
+                bv = sv[i];
                 bi = e;
             }
         }
         warp_argmax(bv, bi);
         if (j < k) {
+            // the probability of the chosen expert, from the lane that holds it
+            float pv = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; i++)
+                if (i == (bi >> 5)) pv = v[i];
+            pv = __shfl_sync(0xffffffffu, pv, bi & 31);
             if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
             if (lane == j) {
-                my_val = bv;
+                my_val = pv;
                 my_idx = bi;
             }
-            sel_sum += bv;   // slot order, identical on every lane
+            sel_sum += pv;   // slot order, identical on every lane
             kth = bv;
         } else if (lane == 0 && gap_out) {
             gap_out[tok] = kth - bv;
@@ -165,7 +181,7 @@ struct Chunk8<float> {
 template <int EP, typename T>
 __global__ void __launch_bounds__(kRouterThreads)
 router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
-                   const float* __restrict__ b_r, int64_t N, int d, int E, int k, int renorm,
+                   const float* __restrict__ b_r, int bias_mode, int64_t N, int d, int E, int k, int renorm,
                    int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                    float* __restrict__ gap_out, float* __restrict__ p_part) {
     __shared__ float sm[kWarps * 32];
@@ -225,7 +241,7 @@ router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
 #pragma unroll
         for (int e = 0; e < EP; e++)
             if (e == lane) v[0] = acc[t][e];
-        finish_token<1>(v, b_r, E, k, renorm, t0 + t, idx_out, w_out, gap_out, pacc);
+        finish_token<1>(v, b_r, bias_mode, E, k, renorm, t0 + t, idx_out, w_out, gap_out, pacc);
     }
     write_p_part<1>(pacc, sm, E, p_part);
 }
@@ -236,7 +252,8 @@ constexpr int kTopkTokensPerBlock = 32;
 
 template <int NV>
 __global__ void __launch_bounds__(kRouterThreads)
-logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b_r, int64_t N,
+logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b_r, int bias_mode,
+                   int64_t N,
                    int E, int k, int renorm, int32_t* __restrict__ idx_out,
                    float* __restrict__ w_out, float* __restrict__ gap_out,
                    float* __restrict__ p_part) {
@@ -254,7 +271,7 @@ logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b
             const int e = lane + 32 * i;
             v[i] = e < E ? logits[tok * E + e] : 0.f;
         }
-        finish_token<NV>(v, b_r, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
+        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
     }
     write_p_part<NV>(pacc, sm, E, p_part);
 }
@@ -277,7 +294,7 @@ struct RouterTile {
 template <int EP, typename T>
 __global__ void __launch_bounds__(kRouterThreads)
 router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
-                    const float* __restrict__ b_r, int64_t N, int d, int E, int k, int renorm,
+                    const float* __restrict__ b_r, int bias_mode, int64_t N, int d, int E, int k, int renorm,
                     int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                     float* __restrict__ gap_out, float* __restrict__ p_part) {
     using Tl = RouterTile<EP>;
@@ -361,7 +378,7 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
         float v[NV];
 #pragma unroll
         for (int i = 0; i < NV; i++) v[i] = Ls[t * (EP + 1) + lane + 32 * i];
-        finish_token<NV>(v, b_r, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
+        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, pacc);
     }
     __syncthreads();             // every warp is done reading the logits
     write_p_part<NV>(pacc, sm, E, p_part);
@@ -391,7 +408,7 @@ template <typename Kernel, typename T>
 void launch_k(Kernel kern, int blocks, cudaStream_t s, const T* x, const float* W_r,
               const float* bias, const moe_cfg& c, int32_t* idx, float* w, float* gap,
               float* p_part) {
-    kern<<<blocks, kRouterThreads, 0, s>>>(x, W_r, bias, c.N, c.d, c.E, c.k, c.renorm, idx, w,
+    kern<<<blocks, kRouterThreads, 0, s>>>(x, W_r, bias, c.bias_mode, c.N, c.d, c.E, c.k, c.renorm, idx, w,
                                            gap, p_part);
 }
 
@@ -415,7 +432,7 @@ template <int NV>
 int launch_topk(const moe_cfg& c, const float* logits, const float* bias, int32_t* idx, float* w,
                 float* gap, float* p_part, cudaStream_t s) {
     const int blocks = (int)((c.N + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
-    logits_topk_kernel<NV><<<blocks, kRouterThreads, 0, s>>>(logits, bias, c.N, c.E, c.k, c.renorm,
+    logits_topk_kernel<NV><<<blocks, kRouterThreads, 0, s>>>(logits, bias, c.bias_mode, c.N, c.E, c.k, c.renorm,
                                                              idx, w, gap, p_part);
     return blocks;
 }
@@ -444,7 +461,7 @@ int64_t router_part_rows(int64_t N) { return (N + 7) / 8 + 1; }
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* p_part, float* P_sum,
                           __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s) {
-    const float* bias = c.bias_mode == 1 ? b_r : nullptr;
+    const float* bias = c.bias_mode != 0 ? b_r : nullptr;
     int blocks = 0;
     if (c.N > 0) {
         if (router_uses_tensor_cores(c)) {

@@ -328,7 +328,8 @@ static __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, vol
 }
 
 // Whole warp, convergent; every lane returns the same answer.
-static __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+static __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             uint64_t timeout_ns = kWaitTimeoutNs) {
     const uint32_t a = smem_u32(bar);
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
@@ -340,7 +341,7 @@ static __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, vol
             if (lane == 0) {
                 uint64_t now = gtimer();
                 if (t0 == 0) t0 = now;
-                stop = (*abort_flag != 0) || (now - t0 > kWaitTimeoutNs);
+                stop = (*abort_flag != 0) || (now - t0 > timeout_ns);
                 if (stop) *abort_flag = 1;
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) return false;

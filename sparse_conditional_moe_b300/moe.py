@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
-           "moe_status_string")
+           "moe_selftest_wait_timeout", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -80,6 +80,7 @@ def lib():
             "moe_forward_buffers": [C, P, SZ, ctypes.POINTER(MoeBuffers)],
             "moe_stats": [C, P, P, P, P, P, P, P, ctypes.POINTER(MoeStatsSummary), P, SZ, P],
             "moe_device_error": [P, SZ, ctypes.POINTER(ctypes.c_int32), P],
+            "moe_selftest_wait_timeout": [P, SZ, ctypes.c_uint32, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -116,10 +117,10 @@ def make_cfg(N: int, d: int, d_ff: int, E: int, k: int, n_shared: int = 0, d_ff_
 
 
 def cfg_from_spec(spec, N: Optional[int] = None) -> MoeCfg:
-    """MoeCfg of a moe_synth.LayerSpec (bias_mode 1 when the layer has a router bias)."""
+    """MoeCfg of a moe_synth.LayerSpec (its bias_mode when the layer has a router bias)."""
     return make_cfg(spec.N if N is None else N, spec.d, spec.d_ff, spec.E, spec.k, spec.n_shared,
                     spec.d_ff_shared, spec.capacity_factor, spec.renorm,
-                    1 if getattr(spec, "zipf_bias", 0) > 0 else 0,
+                    getattr(spec, "bias_mode", 1) if getattr(spec, "zipf_bias", 0) > 0 else 0,
                     MOE_BF16 if spec.dtype == "bf16" else MOE_F32)
 
 
@@ -257,6 +258,12 @@ def moe_stats(cfg, counts, kept, P_sum, pos, gap, ws, stream=None):
     return dict(f=list(f), P=list(P), aux=s.aux, dropped=s.dropped, fully_dropped=s.fully_dropped,
                 near_tie=s.near_tie, touched_experts=s.touched_experts, kept_rows=s.kept_rows,
                 device_error=s.device_error)
+
+
+def moe_selftest_wait_timeout(ws, timeout_us: int, stream=None):
+    """Launch the bounded-wait failure check (see include/moe.h); asynchronous."""
+    _check(lib().moe_selftest_wait_timeout(_p(ws), ws.numel(), timeout_us, _s(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_device_error(ws, stream=None) -> int:

@@ -56,13 +56,14 @@ def internal_tie(probs: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return np.any(np.abs(np.diff(sel, axis=1)) < TIE, axis=1)
 
 
-def check_routing(idx_g, w_g, gap_g, idx_o, w_o, probs_o, gap_o):
+def check_routing(idx_g, w_g, gap_g, idx_o, w_o, probs_o, gap_o, scores_o=None):
     """Bit-exact routing on every token whose expert set is unique; returns (excluded mask,
-    tokens whose GPU routing differs from the oracle's)."""
+    tokens whose GPU routing differs from the oracle's).  scores_o: the selection scores when
+    they are not the probabilities (selection-only bias)."""
     idx_g = np.asarray(idx_g)
     w_g = np.asarray(w_g)
     excl = gap_o < TIE
-    order_tie = internal_tie(probs_o, idx_o)
+    order_tie = internal_tie(probs_o if scores_o is None else scores_o, idx_o)
     strict = ~excl & ~order_tie
     bad = np.nonzero(strict & np.any(idx_g != idx_o, axis=1))[0]
     assert bad.size == 0, f"routing differs on tokens {bad[:10]} ({bad.size})"

@@ -72,7 +72,8 @@ def _status(L, cfg):
 @pytest.mark.parametrize("kw,code", [
     (dict(k=9), 1), (dict(E=0), 1), (dict(k=0), 1), (dict(N=-1), 1), (dict(d=100), 1),
     (dict(d_ff=12), 1), (dict(act_dtype=7), 1), (dict(renorm=2), 1), (dict(n_shared=1, d_ff_shared=0), 1),
-    (dict(E=2048, k=2), 2), (dict(k=17, E=64), 2), (dict(bias_mode=2), 2), (dict(n_shared=9), 2),
+    (dict(E=2048, k=2), 2), (dict(k=17, E=64), 2), (dict(bias_mode=3), 1), (dict(n_shared=9), 2),
+    (dict(bias_mode=2), 0),
     (dict(), 0), (dict(N=0), 0), (dict(act_dtype=moe.MOE_F32, d=100, d_ff=12, d_ff_shared=12), 0),
 ])
 def test_cfg_validation(L, kw, code):

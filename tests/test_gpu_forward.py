@@ -34,7 +34,13 @@ SMALL = [
                         d_ff_shared=64),
     moe_synth.LayerSpec("f32_capacity", N=100, d=64, d_ff=96, E=8, k=3, capacity_factor=0.5,
                         dtype="f32", n_shared=1, d_ff_shared=32),
+    moe_synth.LayerSpec("bf16_selection_bias", N=256, d=512, d_ff=256, E=64, k=6, n_shared=1,
+                        d_ff_shared=128, zipf_bias=1.2, bias_mode=2, capacity_factor=1.5),
 ]
+
+
+def _bias_mode(spec):
+    return spec.bias_mode if spec.zipf_bias > 0 else 0
 
 
 def _by_expert(idx, pos):
@@ -74,10 +80,12 @@ def test_forward_small_layers_every_token(spec):
     assert lay.device_error() == 0
     bufs = lay.buffers()
     code = dtype_code(spec)
-    ref, ex = oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor)
+    ref, ex = oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor,
+                                   bias_mode=_bias_mode(spec))
+    scores = ex["probs"] + L["b_r"].numpy()[None, :] if _bias_mode(spec) == 2 else None
     excl, differs = check_routing(bufs["idx"].cpu().numpy(), bufs["w"].cpu().numpy(),
                                   bufs["gap"].cpu().numpy(), ex["idx"], ex["w"], ex["probs"],
-                                  ex["gap"])
+                                  ex["gap"], scores_o=scores)
     _grouping_checks(spec, bufs, ex["idx"], differs)
     rows = np.ones(spec.N, bool) if differs.size == 0 else ~excl
     compare_rows(out_f64(out, spec), out_f64(ref, spec), spec, rows=rows)

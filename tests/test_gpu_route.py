@@ -71,3 +71,26 @@ def test_route_empty_batch():
     dummy = torch.empty(16, dtype=torch.float32, device="cuda")
     moe.moe_route(cfg, dummy, L["W_r"].cuda(), None, dummy, dummy, P, None, ws)
     assert torch.all(P.cpu() == 0)
+
+
+@pytest.mark.parametrize("N,d,E,k,dt", [
+    (96, 256, 16, 4, "bf16"),      # GEMV router
+    (300, 2048, 128, 8, "bf16"),   # tensor-core router
+    (257, 7168, 256, 8, "bf16"),
+    (64, 128, 64, 6, "f32"),       # fp32 tiled router
+])
+def test_route_selection_only_bias(N, d, E, k, dt):
+    """bias_mode 2 (DeepSeek-V3 balancing bias): top-k chosen on p + b, weights unbiased."""
+    spec = moe_synth.LayerSpec("r2", N=N, d=d, d_ff=64, E=E, k=k, dtype=dt, zipf_bias=1.2,
+                               bias_mode=2)
+    L = moe_synth.make_layer(spec, seed=N + 3 * E, x_only=True)
+    L["b_r"] = L["b_r"] * 0.02          # a bias on the scale of the probabilities
+    idx, w, P, gap = _route(spec, L)
+    idx_o, w_o, probs_o, gap_o = oracle.route(L["x"], L["W_r"], L["b_r"], k, dtype_code(spec),
+                                              bias_mode=2)
+    check_routing(idx, w, gap, idx_o, w_o, probs_o, gap_o,
+                  scores_o=probs_o + L["b_r"].numpy()[None, :])
+    np.testing.assert_allclose(P, probs_o.astype(np.float64).sum(0), rtol=1e-5, atol=1e-6)
+    # the bias really changed the selection on this layer
+    idx_nb = oracle.route(L["x"], L["W_r"], None, k, dtype_code(spec))[0]
+    assert np.any(np.sort(idx_nb, 1) != np.sort(idx_o, 1))

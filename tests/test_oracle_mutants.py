@@ -23,8 +23,8 @@ MUTANTS = {
     "down_transposed": ("elem(Wd, dtype, (int64_t)i * F + n)", "elem(Wd, dtype, (int64_t)n * d + i)"),
     "gate_up_swapped": ("double hv = silu(g) * u;", "double hv = silu(u) * g;"),
     "wrong_slot_weight": ("acc[i] += (double)w_t[j] * y[i];", "acc[i] += (double)w_t[0] * y[i];"),
-    "ties_to_higher_index": ("if (!chosen[e] && (best < 0 || probs[e] > probs[best]))",
-                             "if (!chosen[e] && (best < 0 || probs[e] >= probs[best]))"),
+    "ties_to_higher_index": ("if (!chosen[e] && (best < 0 || sel[e] > sel[best]))",
+                             "if (!chosen[e] && (best < 0 || sel[e] >= sel[best]))"),
     "no_renorm": ("w[j] = renorm ? (float)((double)probs[idx[j]] / ws) : probs[idx[j]];",
                   "w[j] = probs[idx[j]];"),
     "unstable_segments": ("perm[offsets[e] + r] = (int32_t)f;",
@@ -32,7 +32,11 @@ MUTANTS = {
     "capacity_off_by_one": ("pos[f] = (r < kept[e]) ? kept_offsets[e] + r : -1;",
                             "pos[f] = (r <= kept[e] && r < counts[e] - 1) ? kept_offsets[e] + r : -1;"),
     "f_over_N": ("f[e] /= (double)(N * k);", "f[e] /= (double)N;"),
-    "router_bias_ignored": ("double acc = b_r ? (double)b_r[e] : 0.0;", "double acc = 0.0;"),
+    "router_bias_ignored": ("double acc = (b_r && bias_mode == 1) ? (double)b_r[e] : 0.0;",
+                            "double acc = 0.0;"),
+    "selection_bias_ignored": ("sel[e] = (b_r && bias_mode == 2) ? (float)((double)probs[e] + (double)b_r[e]) : probs[e];",
+                               "sel[e] = probs[e];"),
+    "selection_bias_in_weights": ("ws += (double)probs[idx[j]];", "ws += (double)sel[idx[j]];"),
     "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
 }
 

@@ -124,3 +124,46 @@ def test_zipf_bias_values():
     assert abs(float(b[0]) - np.log(1 / H)) < 1e-6
     assert abs(float(b[127]) - np.log(128 ** -1.2 / H)) < 1e-5
     np.testing.assert_allclose(np.exp(b.numpy()).sum(), 1.0, atol=1e-6)
+
+
+# ---------------------------------------------------------------- selection-only bias
+# Page "混合专家 MoE", section "负载均衡": DeepSeek-V3's balancing adds a per-expert bias to
+# the routing score that only decides the top-k and does not change the weights.
+
+def test_selection_bias_picks_by_p_plus_b_weights_stay_unbiased(orc):
+    x, W, _ = _tiny(21, N=30, d=24, E=8)
+    b = torch.tensor([0.0, 0.3, -0.2, 0.05, 0.0, 0.6, -1.0, 0.1])
+    idx, w, probs, gap = orc.route(x, W, b, 3, orc.F32, bias_mode=2)
+    idx0, w0, probs0, gap0 = orc.route(x, W, None, 3, orc.F32)
+    np.testing.assert_array_equal(probs, probs0)            # probabilities unbiased
+    logits = x.to(torch.float64).numpy() @ W.to(torch.float64).numpy().T
+    for t in range(30):
+        score = probs[t].astype(np.float64) + b.double().numpy()
+        best = max(itertools.combinations(range(8), 3), key=lambda s: sum(score[list(s)]))
+        assert sorted(best) == sorted(idx[t].tolist())
+        assert all(score[idx[t, j]] >= score[idx[t, j + 1]] for j in range(2))
+        sel = logits[t, idx[t]]                               # weights: softmax over the
+        ref = np.exp(sel - sel.max()) / np.exp(sel - sel.max()).sum()   # selected logits
+        np.testing.assert_allclose(w[t], ref, atol=1e-6, rtol=0)
+        s = np.sort(score)[::-1]
+        assert abs(gap[t] - (s[2] - s[3])) <= 1e-6
+
+
+def test_selection_bias_zero_equals_no_bias(orc):
+    x, W, _ = _tiny(22, N=20, d=16, E=6)
+    a = orc.route(x, W, torch.zeros(6), 2, orc.F32, bias_mode=2)
+    b = orc.route(x, W, None, 2, orc.F32)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+
+
+def test_large_selection_bias_forces_expert_but_not_its_weight(orc):
+    x, W, _ = _tiny(23, N=25, d=16, E=8)
+    b = torch.zeros(8)
+    b[6] = 10.0
+    idx, w, probs, _ = orc.route(x, W, b, 2, orc.F32, bias_mode=2)
+    assert np.all(idx[:, 0] == 6)
+    # the forced expert's weight is its unbiased share, not ~1 as a logit bias would give
+    np.testing.assert_allclose(w[:, 0], probs[:, 6] / (probs[:, 6] + probs[np.arange(25), idx[:, 1]]),
+                               rtol=1e-6)
+    assert w[:, 0].max() < 0.99
