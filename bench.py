@@ -10,7 +10,8 @@ events; `e2e` repeats the measurement through the same C ABI with the batch copi
 host memory and the output copied back every step.  `roofline` reports the dominant kernel (the
 routed gate/up grouped GEMM) against the measured bf16 peak.  `cpu_baseline` times the CPU oracle
 on a bounded sub-batch of the same layer.  Under torchrun (N > 1) every rank runs its own replica
-(the layer needs no exchange between GPUs).
+(the layer needs no exchange between GPUs).  The W4A16 workload runs moe_forward_w4a16 on expert
+weights quantised once by the library before timing.
 """
 from __future__ import annotations
 
@@ -22,6 +23,8 @@ import subprocess
 import sys
 import threading
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -126,15 +129,59 @@ def cpu_oracle_rate(spec, layer_host: dict, budget_s: float, max_steps: int = 0)
     while True:
         L = dict(layer_host)
         L["x"] = x[start:start + sub]
-        t0 = time.perf_counter()
-        oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor)
-        t_used += time.perf_counter() - t0
+        if spec.w4a16:
+            t_used += _oracle_w4_batch(spec, L)
+        else:
+            t0 = time.perf_counter()
+            oracle.forward_naive(L, spec.k, code, cf=spec.capacity_factor)
+            t_used += time.perf_counter() - t0
         done += L["x"].shape[0]
         steps += 1
         start = (start + sub) % max(1, spec.N - sub + 1)
         if t_used >= budget_s or (max_steps and steps >= max_steps):
             break
     return done / t_used, done, t_used, sub, cores
+
+
+_W4_ORACLE_WEIGHTS = {}
+
+
+def _oracle_w4_batch(spec, L) -> float:
+    """The W4A16 layer on one sub-batch with the oracle: routing, capacity, then every token's
+    experts on the oracle's own quantised weights (quantised once, outside the timed parts).
+    Returns the seconds spent in the timed parts."""
+    import concurrent.futures as cf
+    import oracle
+    cache = _W4_ORACLE_WEIGHTS.setdefault(id(L["W_gate"]), {})
+
+    def trip(prefix, e):
+        if (prefix, e) not in cache:
+            cache[(prefix, e)] = tuple(oracle.quantize_w4(L[prefix + n][e])
+                                       for n in ("_gate", "_up", "_down"))
+        return cache[(prefix, e)]
+
+    t0 = time.perf_counter()
+    idx, w, _, _ = oracle.route(L["x"], L["W_r"], L["b_r"], spec.k, oracle.BF16,
+                                bias_mode=spec.bias_mode if L["b_r"] is not None else None)
+    n = L["x"].shape[0]
+    keep = oracle.keep_naive(idx, spec.E, oracle.capacity(n, spec.k, spec.E,
+                                                          spec.capacity_factor))
+    t_route = time.perf_counter() - t0
+    for e in np.unique(idx):                       # untimed: weight preparation
+        trip("W", int(e))
+    shared = [trip("Ws", s) for s in range(spec.n_shared)]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max(1, min(n, len(os.sched_getaffinity(0))))) as ex:
+        list(ex.map(lambda t: oracle.moe_token_w4(L["x"][t], w[t], keep[t],
+                                                 [trip("W", int(e)) for e in idx[t]], shared, 1),
+                    range(n)))
+    return t_route + time.perf_counter() - t0
+
+
+def metric_name(spec) -> str:
+    if spec == moe_synth.MIXTRAL:
+        return "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
+    return f"MoE layer forward tokens/s ({spec.name})"
 
 
 def host_layer(dev: dict) -> dict:
@@ -177,7 +224,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = moe_synth.make_layer(spec, seed=0, device="cuda")
     cfg = moe.cfg_from_spec(spec)
-    lay = moe.MoELayer(cfg, dev)
+    w4 = moe.quantize_layer_w4(dev) if spec.w4a16 else None
+    lay = moe.MoELayer(cfg, dev, w4=w4)
     xs = [dev["x"], moe_synth.make_x(spec, seed=1000 + rank, device="cuda")]
     stream = torch.cuda.current_stream()
 
@@ -225,16 +273,18 @@ def main():
 
     # ---------------- roofline of the dominant kernel (routed gate/up grouped GEMM)
     act_b = 2 if spec.dtype == "bf16" else 4
+    w_b = accounting.W4_BYTES_PER_WEIGHT if spec.w4a16 else act_b
     gu_flops = accounting.gateup_flops(spec.d, spec.d_ff, kept_rows)
     gu_s = ph_ms["gateup"] / 1e3
     peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     achieved_t = gu_flops / gu_s / 1e12
     work = accounting.layer_work(spec.N, spec.d, spec.d_ff, spec.E, spec.k, spec.n_shared,
-                                 spec.d_ff_shared, act_b, kept_rows, touched)
+                                 spec.d_ff_shared, act_b, kept_rows, touched, weight_bytes=w_b)
     layer_tflops = work.flops / (ms_step / 1e3) / 1e12
     layer_gbs = work.bytes / (ms_step / 1e3) / 1e9
     roof_s = work.roofline_s(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
     traffic = read_traffic("gateup")
+    phase_roof = phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks)
 
     # ---------------- end to end through the C ABI with host buffers
     x_host = [x.cpu().pin_memory() for x in xs]
@@ -260,7 +310,10 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = spec.N * world / (e2e_ms / 1e3)
 
-    launches_per_step = 2 + 4 + 1 + 2 + (2 if spec.n_shared > 0 else 0) + 1
+    # router 2, permute 4, m-tile plan 1 (not on the W4A16 path), routed 2, shared 2, combine 1
+    launches_per_step = 2 + 4 + (0 if spec.w4a16 else 1) + 2 + (2 if spec.n_shared > 0 else 0) + 1
+    gemm_kernel = ("grouped W4A16 gate/up SwiGLU (CUDA cores, FFMA2)" if spec.w4a16
+                   else "grouped gate/up SwiGLU GEMM (tcgen05)")
 
     # ---------------- CPU oracle on a bounded sub-batch (rank 0 only)
     cpu = None
@@ -268,12 +321,13 @@ def main():
         rate, done, secs, sub, cores = cpu_oracle_rate(spec, host_layer(dev), args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{done} tokens of {spec.name} in consecutive sub-batches of {sub} "
-                         f"(each its own batch), {secs:.1f} s of CPU work"}
+                         f"(each its own batch), {secs:.1f} s of CPU work"
+                         + (" (weights quantised by the oracle beforehand, untimed)"
+                            if spec.w4a16 else "")}
 
     if rank == 0:
         line = {
-            "metric": "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
-            if spec == moe_synth.MIXTRAL else f"MoE layer forward tokens/s ({spec.name})",
+            "metric": metric_name(spec),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if act_b == 2 else "f32",
@@ -281,18 +335,27 @@ def main():
             "config": {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff,
                        "E": spec.E, "k": spec.k, "n_shared": spec.n_shared,
                        "capacity_factor": spec.capacity_factor,
+                       "weights": "w4a16 (int4 codes + fp32 scale per 128)" if spec.w4a16
+                       else spec.dtype,
                        "l2": "no flush: weights of %.2f GB exceed the 126 MB L2" %
-                             (3 * spec.E * spec.d * spec.d_ff * act_b / 1e9),
+                             (3 * spec.E * spec.d * spec.d_ff * w_b / 1e9),
                        "parallelism": f"replicas x{world}"},
             "layer": {"tflops": layer_tflops, "hbm_gbs_alg": layer_gbs,
                       "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s * 1e3 / ms_step,
                       "kept_rows": kept_rows, "touched_experts": touched,
-                      "phase_ms": ph_ms},
-            "roofline": {"kernel": "grouped gate/up SwiGLU GEMM (tcgen05)", "bound": "tensor",
-                         "achieved": achieved_t, "peak": peak_t, "unit": "TFLOP/s",
-                         "frac": achieved_t / peak_t, "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a "
-                                        f"continuous loop); burst {peaks['bf16_tflops']}"},
+                      "phase_ms": ph_ms, "phase_roofline": phase_roof},
+            "roofline": ({"kernel": gemm_kernel, "bound": "tensor",
+                          "achieved": achieved_t, "peak": peak_t, "unit": "TFLOP/s",
+                          "frac": achieved_t / peak_t, "traffic": traffic,
+                          "frac_of_burst": achieved_t / peaks["bf16_tflops"],
+                          "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a "
+                                         f"continuous loop); burst {peaks['bf16_tflops']}"}
+                         if phase_roof["gateup"]["unit"] == "TFLOP/s" else
+                         {"kernel": gemm_kernel, "bound": "hbm",
+                          "achieved": phase_roof["gateup"]["achieved"], "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": phase_roof["gateup"]["frac"],
+                          "traffic": None if spec.w4a16 else traffic,
+                          "peak_source": f"{peak_src} HBM copy bandwidth"}),
             "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": spec.N * spec.d * act_b,
@@ -303,6 +366,39 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks):
+    """Achieved rate of every phase against its own bound (algorithmic work only): the GEMM
+    phases in TFLOP/s against the bf16 peak, the data-movement phases in GB/s against HBM.
+    w_b: bytes per expert weight (the activation size, or 0.53125 for W4A16)."""
+    d, F, E, N, S, Fs = spec.d, spec.d_ff, spec.E, spec.N, spec.n_shared, spec.d_ff_shared
+    tf_peak, gb_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), peaks["hbm_gbs"]
+    w_bytes = w_b * d * F
+    work = {
+        # x read + W_r read
+        "route": ("GB/s", N * d * act_b + 4.0 * d * E),
+        # x rows read + grouped rows written (+ indices)
+        "permute": ("GB/s", 2.0 * kept_rows * d * act_b + 16.0 * N * spec.k),
+        "gateup": ("TFLOP/s", accounting.gateup_flops(d, F, kept_rows)),
+        "down": ("TFLOP/s", accounting.down_flops(d, F, kept_rows)),
+        "shared": ("TFLOP/s", 6.0 * d * Fs * N * S),
+        # grouped rows + shared rows read, out written
+        "combine": ("GB/s", (kept_rows + S * N) * d * act_b + N * d * act_b),
+    }
+    if spec.N <= 1024:   # decode-sized: the GEMMs stream weights, HBM is their bound
+        work["gateup"] = ("GB/s", 2.0 * w_bytes * touched + kept_rows * (d + F) * act_b)
+        work["down"] = ("GB/s", 1.0 * w_bytes * touched + kept_rows * (d + F) * act_b)
+        work["shared"] = ("GB/s", 3.0 * w_b * d * Fs * S + N * (d + Fs) * act_b * 2)
+    out = {}
+    for ph, (unit, amount) in work.items():
+        ms = ph_ms.get(ph, 0.0)
+        if ms <= 0 or amount <= 0:
+            continue
+        rate = amount / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        peak = tf_peak if unit == "TFLOP/s" else gb_peak
+        out[ph] = {"ms": ms, "achieved": rate, "unit": unit, "frac": rate / peak}
+    return out
 
 
 def read_traffic(kernel: str):
@@ -342,7 +438,7 @@ def run_reference(args, spec, rank, world):
     wall = time.perf_counter() - t0
     value = total / secs_total
     line = {
-        "impl": "reference", "metric": "MoE layer forward tokens/s", "value": value,
+        "impl": "reference", "metric": metric_name(spec), "value": value,
         "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * spec.N / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",

@@ -224,6 +224,64 @@ typedef struct {
 
 MOE_API moe_status moe_forward_buffers(const moe_cfg *cfg, void *ws, size_t ws_bytes, moe_buffers *out_host);
 
+/* ------------------------------------------------------------------ W4A16 expert weights */
+
+/*
+ * W4A16 ("混合专家模型 (MoE)：大规模稀疏条件计算的架构与工程实践", section 五.1, the VRAM wall:
+ * only the expert layers are quantised, weights to INT4 with 16-bit activations, and the
+ * arithmetic runs on dequantised values).  The page fixes no format; this library's is symmetric
+ * per-group INT4: for a weight matrix [rows, cols] (cols a multiple of MOE_W4_GROUP), each row's
+ * groups of MOE_W4_GROUP consecutive columns share one fp32 scale s = max|w| / 7 (fp32
+ * division), stored group-major: s[g * rows + r] for row r, group g; a weight's code is
+ * q = w / s rounded half to even and clamped to [-8, 7] (0 when s == 0), stored as a
+ * two's-complement nibble, two per byte, the even column in the low nibble.  The dequantised
+ * weight is q * s.  Activations, h and the output stay bf16 (act_dtype MOE_BF16
+ * only); d, d_ff and d_ff_shared must be multiples of MOE_W4_GROUP.
+ */
+#define MOE_W4_GROUP 128
+
+typedef struct {
+    const uint8_t *q;   /* device, [rows, cols/2] packed codes, 16-byte aligned */
+    const float *s;     /* device, [cols/MOE_W4_GROUP, rows] fp32 scales, 16-byte aligned */
+} moe_w4;
+
+/* The quantised expert weights of a layer, in the layouts of moe_forward's bf16 weights
+ * (rows x cols): gate, up [E*d_ff, d]; down [E*d, d_ff]; shared_gate, shared_up [S*d_ff_shared, d];
+ * shared_down [S*d, d_ff_shared] (shared_* ignored when n_shared == 0). */
+typedef struct {
+    moe_w4 gate, up, down;
+    moe_w4 shared_gate, shared_up, shared_down;
+} moe_w4_layer;
+
+/*
+ * moe_quantize_w4 -- W [rows, cols] bf16 (device) -> q [rows, cols/2], s [cols/128, rows]
+ * (device, caller-owned) in the format above; codes are bit-exact with its definition.
+ * cols must be a positive multiple of MOE_W4_GROUP (else MOE_ERR_INVALID_ARG); rows >= 0.
+ * Asynchronous on stream.
+ */
+MOE_API moe_status moe_quantize_w4(const void *W, int64_t rows, int32_t cols, uint8_t *q,
+                                   float *s, void *stream);
+
+/*
+ * moe_grouped_ffn_w4a16 -- moe_grouped_ffn with W4A16 routed-expert weights (W->gate, up,
+ * down; the shared_* members are not read).  Arguments otherwise as in moe_grouped_ffn.
+ * Returns MOE_ERR_UNSUPPORTED unless act_dtype is MOE_BF16 and d, d_ff are multiples of 128.
+ */
+MOE_API moe_status moe_grouped_ffn_w4a16(const moe_cfg *cfg, const void *x_perm,
+                                         const int32_t *kept, const int32_t *kept_offsets,
+                                         const float *row_weight, const moe_w4_layer *W_host,
+                                         void *y_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_forward_w4a16 -- moe_forward with W4A16 expert weights (routed and shared), the router
+ * unchanged (fp32 W_r).  W_host is a host pointer to the struct of device pointers.
+ * events: NULL, or MOE_TRACE_EVENTS events recorded as in moe_forward_traced.
+ */
+MOE_API moe_status moe_forward_w4a16(const moe_cfg *cfg, const void *x, const float *W_r,
+                                     const float *b_r, const moe_w4_layer *W_host, void *out,
+                                     void *ws, size_t ws_bytes, void *stream,
+                                     void *const *events);
+
 /* ------------------------------------------------------------------ statistics */
 
 /* Load-balance statistics ("混合专家 MoE", 负载均衡 section, aux_loss). */

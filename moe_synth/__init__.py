@@ -42,6 +42,7 @@ class LayerSpec:
     zipf_bias: float = 0.0         # > 0: router bias ln Zipf(s) over expert rank
     renorm: int = 1
     bias_mode: int = 1             # how a router bias enters: 1 logits, 2 top-k choice only
+    w4a16: bool = False            # expert weights run as 4-bit codes + per-128 scales
 
     def with_(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)
@@ -54,12 +55,14 @@ MIXTRAL = LayerSpec("mixtral_8x_bf16", N=4096, d=4096, d_ff=14336, E=8, k=2)
 DSV3_PREFILL = LayerSpec("deepseek_v3_prefill_bf16", N=8192, d=7168, d_ff=2048,
                          E=256, k=8, n_shared=1, d_ff_shared=2048)
 DSV3_DECODE = DSV3_PREFILL.with_(name="deepseek_v3_decode_bf16", N=64)
+DSV3_DECODE_W4 = DSV3_DECODE.with_(name="deepseek_v3_decode_w4a16", w4a16=True)
 QWEN3_SKEWED = LayerSpec("qwen3_30b_a3b_skewed_bf16", N=16384, d=2048, d_ff=768,
                          E=128, k=8, capacity_factor=1.25, zipf_bias=1.2)
 PAGE_SELFTEST = LayerSpec("page_selftest_fp32", N=50, d=64, d_ff=128, E=16, k=4,
                           n_shared=1, d_ff_shared=128, dtype=F32)
 
-WORKLOADS = {s.name: s for s in (TINY, MIXTRAL, DSV3_PREFILL, DSV3_DECODE, QWEN3_SKEWED)}
+WORKLOADS = {s.name: s for s in (TINY, MIXTRAL, DSV3_PREFILL, DSV3_DECODE, QWEN3_SKEWED,
+                                  DSV3_DECODE_W4)}
 
 
 def zipf_bias(E: int, s: float) -> torch.Tensor:

@@ -23,8 +23,14 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _OVERRIDE = os.environ.get("MOE_ORACLE_LIB")
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, W4 = 0, 1, 2
+W4_GROUP = 128
 TIE_EPS = 1e-6
+
+
+class W4Mat(ctypes.Structure):
+    """A W4A16 weight matrix as the oracle reads it: packed 4-bit codes and fp32 group scales."""
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("rows", ctypes.c_int64)]
 
 
 def build(force: bool = False) -> str:
@@ -54,12 +60,18 @@ def lib():
         L.oracle_keep_naive.restype = None
         L.oracle_moe_token.argtypes = [I32, I32, I32, I32, I32, I32, I32, P, P, P,
                                        P, P, P, P, P, P, P]
+        L.oracle_moe_token_w.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32, P, P, P,
+                                         P, P, P, P, P, P, P]
+        L.oracle_quantize_w4.argtypes = [P, I64, I32, P, P]
+        L.oracle_dequantize_w4.argtypes = [P, P, I64, I32, P]
+        L.oracle_dequantize_w4.restype = None
         L.oracle_forward_naive.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
                                            P, P, P, I32, P, P, P, P, P, P, P, P, P, P, P, P]
         L.oracle_forward_grouped.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
                                              P, P, P, I32, P, P, P, P, P, P, P]
         L.oracle_stats.argtypes = [I64, I32, I32, P, P, P, P, D, P, P, P, P]
-        for fn in ("oracle_route", "oracle_permute", "oracle_moe_token", "oracle_forward_naive",
+        for fn in ("oracle_route", "oracle_permute", "oracle_moe_token", "oracle_moe_token_w",
+                   "oracle_quantize_w4", "oracle_forward_naive",
                    "oracle_forward_grouped", "oracle_stats"):
             getattr(L, fn).restype = I32
         _lib = L
@@ -177,6 +189,59 @@ def moe_token(x_t, w_t, keep_t, experts: Sequence, shared: Sequence, dtype: int,
                                 ptrs(smats, 0), ptrs(smats, 1), ptrs(smats, 2), _p(out))
     if rc:
         raise ValueError("oracle_moe_token rejected its arguments")
+    return out
+
+
+def quantize_w4(W, cols: Optional[int] = None):
+    """bf16 weight rows -> (q uint8 [rows, cols/2], s float32 [cols/128, rows]) (W4A16 format,
+    scales group-major)."""
+    Wb = as_host(W, BF16)
+    cols = Wb.shape[-1] if cols is None else cols
+    Wb = np.ascontiguousarray(Wb.reshape(-1, cols))
+    rows = Wb.shape[0]
+    q = np.zeros((rows, cols // 2), np.uint8)
+    s = np.zeros((cols // W4_GROUP, rows), np.float32)
+    if lib().oracle_quantize_w4(_p(Wb), rows, cols, _p(q), _p(s)):
+        raise ValueError("oracle_quantize_w4: cols must be a multiple of 128")
+    return q, s
+
+
+def dequantize_w4(q, s, cols: int) -> np.ndarray:
+    """(q [rows, cols/2], s [cols/128, rows]) -> W [rows, cols] float64, exactly q * s."""
+    q = np.ascontiguousarray(q, np.uint8).reshape(-1, cols // 2)
+    s = np.ascontiguousarray(s, np.float32).reshape(cols // W4_GROUP, q.shape[0])
+    W = np.zeros((q.shape[0], cols), np.float64)
+    lib().oracle_dequantize_w4(_p(q), _p(s), q.shape[0], cols, _p(W))
+    return W
+
+
+def moe_token_w4(x_t, w_t, keep_t, experts: Sequence, shared: Sequence, round_h: int = 1):
+    """One token's layer output (bf16 bits) with W4A16 weights.  experts / shared: tuples of
+    ((q, s) gate, (q, s) up, (q, s) down) per chosen / shared expert, in slot order."""
+    x_t = as_host(x_t, BF16)
+    d = x_t.shape[-1]
+    keep = []
+
+    def mats(trips, i):
+        arr = (ctypes.c_void_p * max(len(trips), 1))()
+        for j, trip in enumerate(trips):
+            q, sc = (np.ascontiguousarray(a) for a in trip[i])
+            m = W4Mat(q.ctypes.data, sc.ctypes.data, q.shape[0])
+            keep.extend([q, sc, m])
+            arr[j] = ctypes.addressof(m)
+        return arr
+
+    k, S = len(experts), len(shared)
+    F = np.asarray(experts[0][0][0]).shape[0] if k else 0
+    Fs = np.asarray(shared[0][0][0]).shape[0] if S else 0
+    w_t = np.ascontiguousarray(w_t, dtype=np.float32)
+    keep_t = np.ascontiguousarray(keep_t, dtype=np.int32)
+    out = np.zeros(d, np.uint16)
+    rc = lib().oracle_moe_token_w(d, F, k, S, Fs, BF16, W4, round_h, _p(x_t), _p(w_t), _p(keep_t),
+                                  mats(experts, 0), mats(experts, 1), mats(experts, 2),
+                                  mats(shared, 0), mats(shared, 1), mats(shared, 2), _p(out))
+    if rc:
+        raise ValueError("oracle_moe_token_w rejected its arguments")
     return out
 
 

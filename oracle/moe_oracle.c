@@ -40,6 +40,18 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_W4 2    /* weights only: 4-bit codes + one fp32 scale per 128 inputs (orc_w4) */
+
+/* A W4A16 weight matrix [rows, cols]: q packs two signed 4-bit codes per byte (even column in
+ * the low nibble), s holds one fp32 scale per 128 consecutive columns of a row, group-major:
+ * s[g * rows + r] is the scale of row r, columns [128 g, 128 g + 128). */
+typedef struct {
+    const uint8_t *q;
+    const float *s;
+    int64_t rows;
+} orc_w4;
+
+#define ORC_W4_GROUP 128
 
 /* ---------- scalar conversions ---------- */
 
@@ -87,6 +99,19 @@ static double elem(const void *p, int dtype, int64_t i)
     if (dtype == ORC_BF16)
         return bf16_bits_to_double(((const uint16_t *)p)[i]);
     return (double)((const float *)p)[i];
+}
+
+/* element (row, col) of a weight matrix with `cols` columns, stored fp32, bf16 or W4 */
+static double wval(const void *p, int wdtype, int64_t row, int64_t col, int64_t cols)
+{
+    if (wdtype == ORC_W4) {
+        const orc_w4 *m = (const orc_w4 *)p;
+        uint8_t byte = m->q[(row * cols + col) / 2];
+        int nib = (col & 1) ? (byte >> 4) : (byte & 15);
+        int code = nib >= 8 ? nib - 16 : nib;                  /* two's complement, 4 bits */
+        return (double)code * (double)m->s[(col / ORC_W4_GROUP) * m->rows + row];
+    }
+    return elem(p, wdtype, row * cols + col);
 }
 
 /* ---------- router: logits, softmax, top-k, renormalise ([H] MoE.route) ---------- */
@@ -254,8 +279,8 @@ static void swiglu_expert(const double *xt, int d, int F, int dtype, const void 
     for (int n = 0; n < F; n++) {
         double g = 0.0, u = 0.0;
         for (int i = 0; i < d; i++) {
-            g += elem(Wg, dtype, (int64_t)n * d + i) * xt[i];
-            u += elem(Wu, dtype, (int64_t)n * d + i) * xt[i];
+            g += wval(Wg, dtype, n, i, d) * xt[i];
+            u += wval(Wu, dtype, n, i, d) * xt[i];
         }
         double hv = silu(g) * u;
         h[n] = round_h ? round_to_bf16_value(hv) : hv;
@@ -263,7 +288,7 @@ static void swiglu_expert(const double *xt, int d, int F, int dtype, const void 
     for (int i = 0; i < d; i++) {
         double acc = 0.0;
         for (int n = 0; n < F; n++)
-            acc += elem(Wd, dtype, (int64_t)i * F + n) * h[n];
+            acc += wval(Wd, dtype, i, n, F) * h[n];
         y[i] = acc;
     }
     free(h);
@@ -286,11 +311,11 @@ static void store_row(void *out, int dtype, int64_t row, int d, const double *ac
  * [F,d] gate matrix of expert idx_t[j], ...), the S shared experts likewise.
  * x_t [d] and out_t [d] are in the layer dtype.
  */
-int oracle_moe_token(int d, int F, int k, int S, int Fs, int dtype, int round_h,
-                     const void *x_t, const float *w_t, const int32_t *keep_t,
-                     const void *const *Wg_k, const void *const *Wu_k, const void *const *Wd_k,
-                     const void *const *Wsg, const void *const *Wsu, const void *const *Wsd,
-                     void *out_t)
+int oracle_moe_token_w(int d, int F, int k, int S, int Fs, int dtype, int wdtype, int round_h,
+                       const void *x_t, const float *w_t, const int32_t *keep_t,
+                       const void *const *Wg_k, const void *const *Wu_k, const void *const *Wd_k,
+                       const void *const *Wsg, const void *const *Wsu, const void *const *Wsd,
+                       void *out_t)
 {
     double *xt = (double *)malloc(sizeof(double) * (size_t)d);
     double *acc = (double *)calloc((size_t)d, sizeof(double));
@@ -300,12 +325,12 @@ int oracle_moe_token(int d, int F, int k, int S, int Fs, int dtype, int round_h,
     for (int j = 0; j < k; j++) {
         if (!keep_t[j])
             continue;
-        swiglu_expert(xt, d, F, dtype, Wg_k[j], Wu_k[j], Wd_k[j], round_h, y);
+        swiglu_expert(xt, d, F, wdtype, Wg_k[j], Wu_k[j], Wd_k[j], round_h, y);
         for (int i = 0; i < d; i++)
             acc[i] += (double)w_t[j] * y[i];
     }
     for (int s = 0; s < S; s++) {
-        swiglu_expert(xt, d, Fs, dtype, Wsg[s], Wsu[s], Wsd[s], round_h, y);
+        swiglu_expert(xt, d, Fs, wdtype, Wsg[s], Wsu[s], Wsd[s], round_h, y);
         for (int i = 0; i < d; i++)
             acc[i] += y[i];
     }
@@ -314,6 +339,17 @@ int oracle_moe_token(int d, int F, int k, int S, int Fs, int dtype, int round_h,
     free(acc);
     free(y);
     return 0;
+}
+
+/* oracle_moe_token_w with the weights in the activation dtype */
+int oracle_moe_token(int d, int F, int k, int S, int Fs, int dtype, int round_h,
+                     const void *x_t, const float *w_t, const int32_t *keep_t,
+                     const void *const *Wg_k, const void *const *Wu_k, const void *const *Wd_k,
+                     const void *const *Wsg, const void *const *Wsu, const void *const *Wsd,
+                     void *out_t)
+{
+    return oracle_moe_token_w(d, F, k, S, Fs, dtype, dtype, round_h, x_t, w_t, keep_t, Wg_k, Wu_k,
+                              Wd_k, Wsg, Wsu, Wsd, out_t);
 }
 
 static const void *expert_mat(const void *bank, int dtype, int64_t e, int64_t rows, int64_t cols)
@@ -510,4 +546,55 @@ int oracle_stats(int64_t N, int E, int k, const int32_t *idx, const float *probs
             counters[2]++;
     }
     return 0;
+}
+
+/* ---------- W4A16 weights ([N] 五.1: INT4 weights, BF16 activations, dequantise then compute) ---------- */
+
+/*
+ * oracle_quantize_w4: W [rows, cols] bf16 bits -> q [rows, cols/2] packed codes, s [cols/128, rows].
+ * Per group of 128 consecutive columns: s = max|w| / 7 (fp32), code = w / s rounded to the nearest
+ * integer (ties to even, fp32 division), clamped to [-8, 7]; an all-zero group has s = 0 and codes 0.
+ * cols must be a multiple of 128.  Returns 1 on bad sizes.
+ */
+int oracle_quantize_w4(const uint16_t *W, int64_t rows, int cols, uint8_t *q, float *s)
+{
+    if (rows < 0 || cols <= 0 || cols % ORC_W4_GROUP)
+        return 1;
+    const int groups = cols / ORC_W4_GROUP;
+    for (int64_t r = 0; r < rows; r++)
+        for (int g = 0; g < groups; g++) {
+            float mx = 0.0f;
+            for (int c = 0; c < ORC_W4_GROUP; c++) {
+                float v = (float)bf16_bits_to_double(W[r * cols + g * ORC_W4_GROUP + c]);
+                if (fabsf(v) > mx)
+                    mx = fabsf(v);
+            }
+            float sc = mx / 7.0f;
+            s[(int64_t)g * rows + r] = sc;
+            for (int c = 0; c < ORC_W4_GROUP; c++) {
+                int64_t col = (int64_t)g * ORC_W4_GROUP + c;
+                float v = (float)bf16_bits_to_double(W[r * cols + col]);
+                int code = 0;
+                if (sc > 0.0f) {
+                    float t = nearbyintf(v / sc);
+                    code = t < -8.0f ? -8 : (t > 7.0f ? 7 : (int)t);
+                }
+                uint8_t nib = (uint8_t)(code & 15);
+                uint8_t *byte = &q[(r * cols + col) / 2];
+                if (col & 1)
+                    *byte = (uint8_t)((*byte & 0x0F) | (nib << 4));
+                else
+                    *byte = (uint8_t)((*byte & 0xF0) | nib);
+            }
+        }
+    return 0;
+}
+
+/* oracle_dequantize_w4: W[r, c] = code * s, exact, in fp64. */
+void oracle_dequantize_w4(const uint8_t *q, const float *s, int64_t rows, int cols, double *W)
+{
+    orc_w4 m = {q, s, rows};
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++)
+            W[r * cols + c] = wval(&m, ORC_W4, r, c, cols);
 }

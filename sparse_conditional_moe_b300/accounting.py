@@ -38,12 +38,19 @@ class Work:
         return "tensor" if self.flops / peak_flops >= self.bytes / peak_bytes else "hbm"
 
 
+# W4A16 expert weights: half a byte per code + one fp32 scale per 128 weights.
+W4_BYTES_PER_WEIGHT = 0.5 + 4.0 / 128
+
+
 def layer_work(N: int, d: int, d_ff: int, E: int, k: int, n_shared: int, d_ff_shared: int,
-               act_bytes: int, kept_assignments: int, touched_experts: int) -> Work:
+               act_bytes: int, kept_assignments: int, touched_experts: int,
+               weight_bytes: float = 0.0) -> Work:
+    """weight_bytes: bytes per expert weight (default: the activation size)."""
+    wb = weight_bytes or act_bytes
     flops = (6.0 * d * d_ff * kept_assignments + 6.0 * d * d_ff_shared * n_shared * N
              + 2.0 * d * E * N)
-    byts = (3.0 * d * d_ff * act_bytes * touched_experts
-            + 3.0 * d * d_ff_shared * act_bytes * n_shared
+    byts = (3.0 * d * d_ff * wb * touched_experts
+            + 3.0 * d * d_ff_shared * wb * n_shared
             + 4.0 * d * E + 2.0 * N * d * act_bytes)
     return Work(flops, byts)
 

@@ -250,6 +250,75 @@ moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int
     return MOE_OK;
 }
 
+// ------------------------------------------------------------------ W4A16 pieces
+
+moe_status check_w4_cfg(const moe_cfg* c) {
+    if (c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->d % kW4GroupK || c->d_ff % kW4GroupK || (c->n_shared > 0 && c->d_ff_shared % kW4GroupK))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status need_w4(const moe_w4& m) {
+    MOE_TRY(need(m.q, 16));
+    return need(m.s, 16);
+}
+
+moe_status check_w4_layer(const moe_cfg* c, const moe_w4_layer* W, bool shared) {
+    if (!W) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(need_w4(W->gate));
+    MOE_TRY(need_w4(W->up));
+    MOE_TRY(need_w4(W->down));
+    if (shared && c->n_shared > 0) {
+        MOE_TRY(need_w4(W->shared_gate));
+        MOE_TRY(need_w4(W->shared_up));
+        MOE_TRY(need_w4(W->shared_down));
+    }
+    return MOE_OK;
+}
+
+W4Mat w4m(const moe_w4& m) { return W4Mat{m.q, m.s}; }
+
+moe_status do_grouped_ffn_w4(const moe_cfg* c, const void* x_perm, const int32_t* kept,
+                             const int32_t* kept_offsets, const float* row_weight,
+                             const moe_w4_layer& W, void* y_perm, void* ws, cudaStream_t s,
+                             void* const* ev) {
+    const WsLayout L = ws_layout(*c);
+    W4Group g{c->E, kept, kept_offsets, 0, 0, 0};
+    auto* h = at<__nv_bfloat16>(ws, L.h_perm);
+    if (grouped_rows(*c) > 0)
+        MOE_CUDA(w4_gateup(g, (const __nv_bfloat16*)x_perm, c->d, w4m(W.gate), w4m(W.up), c->d_ff,
+                           h, at<int32_t>(ws, L.err), grouped_rows(*c), s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
+    if (grouped_rows(*c) > 0)
+        MOE_CUDA(w4_down(g, h, c->d_ff, w4m(W.down), c->d, row_weight, (__nv_bfloat16*)y_perm,
+                         at<int32_t>(ws, L.err), grouped_rows(*c), s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
+    return MOE_OK;
+}
+
+moe_status do_shared_w4_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
+                                    const void* x, const moe_w4_layer& W, void* out, void* ws,
+                                    cudaStream_t s, void* const* ev) {
+    const WsLayout L = ws_layout(*c);
+    auto* hsh = at<__nv_bfloat16>(ws, L.h_sh);
+    auto* ysh = at<__nv_bfloat16>(ws, L.y_sh);
+    if (c->n_shared > 0 && c->N > 0) {
+        // every shared expert reads all N tokens of x; its h and y blocks are N rows apart
+        W4Group g{c->n_shared, nullptr, nullptr, (int)c->N, 0, c->N};
+        MOE_CUDA(w4_gateup(g, (const __nv_bfloat16*)x, c->d, w4m(W.shared_gate),
+                           w4m(W.shared_up), c->d_ff_shared, hsh, at<int32_t>(ws, L.err),
+                           c->N * c->n_shared, s));
+        g.a_stride = c->N;
+        MOE_CUDA(w4_down(g, hsh, c->d_ff_shared, w4m(W.shared_down), c->d, nullptr, ysh,
+                         at<int32_t>(ws, L.err), c->N * c->n_shared, s));
+    }
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
+    MOE_CUDA(launch_combine(*c, y_perm, pos, ysh, out, at<int32_t>(ws, L.err), s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
+    return MOE_OK;
+}
+
 moe_status check_weights(const moe_cfg* c, const void* Wg, const void* Wu, const void* Wd) {
     MOE_TRY(need(Wg, 16));
     MOE_TRY(need(Wu, 16));
@@ -431,6 +500,74 @@ moe_status moe_forward(const moe_cfg* cfg, const void* x, const float* W_r, cons
                        void* ws, size_t ws_bytes, void* stream) {
     return moe_forward_traced(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, out,
                               ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_quantize_w4(const void* W, int64_t rows, int32_t cols, uint8_t* q, float* s,
+                           void* stream) {
+    if (rows < 0 || cols <= 0 || cols % kW4GroupK) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (rows * (int64_t)cols >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(need(W, 16));
+    MOE_TRY(need(q, 16));
+    MOE_TRY(need(s, 16));
+    MOE_CUDA(w4_quantize((const __nv_bfloat16*)W, rows, cols, q, s, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_grouped_ffn_w4a16(const moe_cfg* cfg, const void* x_perm, const int32_t* kept,
+                                 const int32_t* kept_offsets, const float* row_weight,
+                                 const moe_w4_layer* W, void* y_perm, void* ws, size_t ws_bytes,
+                                 void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_w4_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(kept, 4));
+    MOE_TRY(need(kept_offsets, 4));
+    MOE_TRY(check_w4_layer(cfg, W, false));
+    if (grouped_rows(*cfg) > 0) {
+        MOE_TRY(need(x_perm, 16));
+        MOE_TRY(need(y_perm, 16));
+        if (row_weight) MOE_TRY(need(row_weight, 4));
+    }
+    return do_grouped_ffn_w4(cfg, x_perm, kept, kept_offsets, row_weight, *W, y_perm, ws,
+                             (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
+                             const moe_w4_layer* W, void* out, void* ws, size_t ws_bytes,
+                             void* stream, void* const* ev) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_w4_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(W_r, 16));
+    if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
+    MOE_TRY(check_w4_layer(cfg, W, true));
+    if (cfg->N > 0) {
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(out, 16));
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(*cfg);
+    int32_t* err = at<int32_t>(ws, L.err);
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
+                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum),
+                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
+    MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
+                            at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                            at<int32_t>(ws, L.kept), at<int32_t>(ws, L.kept_offsets),
+                            at<int32_t>(ws, L.perm), at<int32_t>(ws, L.pos),
+                            at<int32_t>(ws, L.row_token), at<float>(ws, L.row_weight),
+                            at<void>(ws, L.x_perm), at<int32_t>(ws, L.blk_hist),
+                            at<int32_t>(ws, L.blk_base), err, s));
+    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
+    MOE_TRY(do_grouped_ffn_w4(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
+                              at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), *W,
+                              at<void>(ws, L.y_perm), ws, s, ev));
+    MOE_TRY(do_shared_w4_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, *W,
+                                     out, ws, s, ev));
+    return MOE_OK;
 }
 
 moe_status moe_forward_buffers(const moe_cfg* cfg, void* ws, size_t ws_bytes, moe_buffers* out) {

@@ -113,6 +113,29 @@ cudaError_t simt_gateup_f32(const GroupGeom& g, const float* A, int K, const flo
 cudaError_t simt_down_f32(const GroupGeom& g, const float* H, int F, const float* Wd, int D,
                           const float* row_scale, float* Y, cudaStream_t s);
 
+// W4A16 expert FFNs (see w4a16.cu): 4-bit codes + fp32 scale per 128 inputs.
+struct W4Mat {
+    const uint8_t* q;   // [rows, K/2]
+    const float* s;     // [K/128, rows] (group-major)
+};
+struct W4Group {
+    int G;
+    const int32_t* rows;      // [G] device, or nullptr for uniform rows
+    const int32_t* row_off;   // [G] device, or nullptr
+    int uniform_rows;
+    int64_t a_stride, c_stride;
+};
+constexpr int kW4GroupK = 128;
+cudaError_t w4_quantize(const __nv_bfloat16* W, int64_t rows, int cols, uint8_t* q, float* s,
+                        cudaStream_t st);
+// total_rows: rows over all groups (sizes the split of token passes across blocks).
+cudaError_t w4_gateup(const W4Group& g, const __nv_bfloat16* A, int K, const W4Mat& Wg,
+                      const W4Mat& Wu, int F, __nv_bfloat16* H, int32_t* err, int64_t total_rows,
+                      cudaStream_t s);
+cudaError_t w4_down(const W4Group& g, const __nv_bfloat16* H, int F, const W4Mat& Wd, int D,
+                    const float* row_scale, __nv_bfloat16* Y, int32_t* err, int64_t total_rows,
+                    cudaStream_t s);
+
 cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* pos,
                            const void* y_sh, void* out, int32_t* err, cudaStream_t s);
 

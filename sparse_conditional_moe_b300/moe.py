@@ -12,7 +12,8 @@ from typing import Optional
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmoe.so")
+# MOE_LIB: load another build of the same library (e.g. one compiled with other tile sizes)
+LIB_PATH = os.environ.get("MOE_LIB") or os.path.join(_PKG, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEVERR_BOUNDS, MOE_DEVERR_TIMEOUT = 1, 2
@@ -24,7 +25,9 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
-           "moe_selftest_wait_timeout", "moe_status_string")
+           "moe_selftest_wait_timeout", "moe_status_string", "moe_quantize_w4",
+           "moe_grouped_ffn_w4a16", "moe_forward_w4a16")
+MOE_W4_GROUP = 128
 
 
 class MoeError(RuntimeError):
@@ -54,6 +57,14 @@ class MoeStatsSummary(ctypes.Structure):
                 ("kept_rows", ctypes.c_int64)]
 
 
+class MoeW4(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p)]
+
+
+class MoeW4Layer(ctypes.Structure):
+    _fields_ = [(n, MoeW4) for n in ("gate", "up", "down", "shared_gate", "shared_up", "shared_down")]
+
+
 _lib = None
 
 
@@ -81,6 +92,9 @@ def lib():
             "moe_stats": [C, P, P, P, P, P, P, P, ctypes.POINTER(MoeStatsSummary), P, SZ, P],
             "moe_device_error": [P, SZ, ctypes.POINTER(ctypes.c_int32), P],
             "moe_selftest_wait_timeout": [P, SZ, ctypes.c_uint32, P],
+            "moe_quantize_w4": [P, I64, ctypes.c_int32, P, P, P],
+            "moe_grouped_ffn_w4a16": [C, P, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P],
+            "moe_forward_w4a16": [C, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -203,14 +217,65 @@ def moe_forward(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
                                  _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down), _p(out), _p(ws),
                                  ws.numel(), _s(stream)), "moe_forward")
     else:
-        for e in events:              # torch creates the CUDA event on its first record
-            if e.cuda_event == 0:
-                e.record(stream if stream is not None else torch.cuda.current_stream())
-        arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        arr = _event_array(events, stream)
         _check(lib().moe_forward_traced(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W_gate),
                                         _p(W_up), _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down),
                                         _p(out), _p(ws), ws.numel(), _s(stream), arr),
                "moe_forward_traced")
+
+
+# ------------------------------------------------------------------ W4A16 expert weights
+
+def moe_quantize_w4(W: torch.Tensor, stream=None):
+    """bf16 W [..., cols] (device) -> (q uint8 [rows, cols/2], s float32 [cols/128, rows]) in the
+    library's W4A16 format (rows = W.numel() / cols; scales group-major)."""
+    cols = W.shape[-1]
+    rows = W.numel() // cols if cols else 0
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=W.device)
+    s = torch.empty((max(cols // MOE_W4_GROUP, 1), rows), dtype=torch.float32, device=W.device)
+    _check(lib().moe_quantize_w4(_p(W), rows, cols, _p(q), _p(s), _s(stream)), "moe_quantize_w4")
+    return q, s
+
+
+def quantize_layer_w4(weights: dict, stream=None) -> dict:
+    """W4A16 copies of a layer's expert weights: {name: (q, s)} for W_gate, W_up, W_down and,
+    when present, Ws_gate, Ws_up, Ws_down."""
+    out = {}
+    for n in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
+        if weights.get(n) is not None:
+            out[n] = moe_quantize_w4(weights[n], stream)
+    return out
+
+
+def w4_layer_struct(w4: dict) -> MoeW4Layer:
+    def m(name):
+        qs = w4.get(name)
+        return MoeW4(None, None) if qs is None else MoeW4(qs[0].data_ptr(), qs[1].data_ptr())
+    return MoeW4Layer(m("W_gate"), m("W_up"), m("W_down"), m("Ws_gate"), m("Ws_up"), m("Ws_down"))
+
+
+def moe_grouped_ffn_w4a16(cfg, x_perm, kept, kept_offsets, row_weight, w4: dict, y_perm, ws,
+                          stream=None):
+    st = w4_layer_struct(w4)
+    _check(lib().moe_grouped_ffn_w4a16(ctypes.byref(cfg), _p(x_perm), _p(kept), _p(kept_offsets),
+                                       _p(row_weight), ctypes.byref(st), _p(y_perm), _p(ws),
+                                       ws.numel(), _s(stream)), "moe_grouped_ffn_w4a16")
+
+
+def _event_array(events, stream):
+    if events is None:
+        return None
+    for e in events:                  # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record(stream if stream is not None else torch.cuda.current_stream())
+    return (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+
+
+def moe_forward_w4a16(cfg, x, W_r, b_r, w4: dict, out, ws, stream=None, events=None):
+    st = w4_layer_struct(w4)
+    _check(lib().moe_forward_w4a16(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(st),
+                                   _p(out), _p(ws), ws.numel(), _s(stream),
+                                   _event_array(events, stream)), "moe_forward_w4a16")
 
 
 def moe_forward_buffers(cfg, ws) -> dict:
@@ -278,9 +343,12 @@ def moe_device_error(ws, stream=None) -> int:
 class MoELayer:
     """Holds device weights, a workspace and an output buffer for one layer shape."""
 
-    def __init__(self, cfg: MoeCfg, weights: dict, device="cuda"):
+    def __init__(self, cfg: MoeCfg, weights: dict, device="cuda", w4: Optional[dict] = None):
+        """w4: W4A16 expert weights (quantize_layer_w4); the forward then reads them instead of
+        the bf16 expert matrices (only W_r and b_r are taken from weights)."""
         self.cfg = cfg
         self.w = weights
+        self.w4 = w4
         self.device = torch.device(device)
         self.ws = workspace(cfg, self.device)
         act = torch.bfloat16 if cfg.act_dtype == MOE_BF16 else torch.float32
@@ -288,6 +356,10 @@ class MoELayer:
 
     def forward(self, x: torch.Tensor, stream=None, events=None) -> torch.Tensor:
         w = self.w
+        if self.w4 is not None:
+            moe_forward_w4a16(self.cfg, x, w["W_r"], w.get("b_r"), self.w4, self.out, self.ws,
+                              stream, events)
+            return self.out
         moe_forward(self.cfg, x, w["W_r"], w.get("b_r"), w["W_gate"], w["W_up"], w["W_down"],
                     w.get("Ws_gate"), w.get("Ws_up"), w.get("Ws_down"), self.out, self.ws,
                     stream, events)

@@ -118,3 +118,65 @@ def test_calls_reject_bad_workspace_and_pointers_without_launching(L):
                        fake_ws, need_b, None) == 1                                   # bias missing
     assert L.moe_grouped_ffn(ctypes.byref(cfg), P(256), P(256), P(256), None, P(256), P(264),
                              P(256), P(256), fake_ws, need, None) == 1                # misaligned W_up
+
+
+def _w4_layer(ptr=256, bad=None):
+    st = moe.MoeW4Layer()
+    for n in ("gate", "up", "down", "shared_gate", "shared_up", "shared_down"):
+        setattr(st, n, moe.MoeW4(ptr, ptr))
+    if bad:
+        setattr(st, bad[0], moe.MoeW4(*bad[1]))
+    return st
+
+
+def test_w4a16_calls_validate_without_launching(L):
+    P = ctypes.c_void_p
+    # quantiser: columns must be a positive multiple of 128; empty input is a no-op
+    assert L.moe_quantize_w4(P(256), 4, 100, P(256), P(256), None) == 1
+    assert L.moe_quantize_w4(P(256), 4, 0, P(256), P(256), None) == 1
+    assert L.moe_quantize_w4(P(256), -1, 128, P(256), P(256), None) == 1
+    assert L.moe_quantize_w4(None, 0, 128, None, None, None) == 0
+    assert L.moe_quantize_w4(P(256), 4, 128, P(264), P(256), None) == 1          # misaligned q
+    cfg = _cfg()
+    need = moe.moe_workspace_size(cfg)
+    fake_ws = P(1 << 20)
+    st = _w4_layer()
+    args = (P(256), P(256), None, ctypes.byref(st), P(256), fake_ws, need, None, None)
+    # fp32 activations, or dims that are not multiples of 128, are not supported
+    f32 = _cfg(act_dtype=moe.MOE_F32)
+    assert L.moe_forward_w4a16(ctypes.byref(f32), *args[:5], fake_ws,
+                               moe.moe_workspace_size(f32), None, None) == 2
+    odd = _cfg(d=136)
+    assert L.moe_forward_w4a16(ctypes.byref(odd), *args[:5], fake_ws,
+                               moe.moe_workspace_size(odd), None, None) == 2
+    odd_ff = _cfg(d_ff=200)
+    assert L.moe_forward_w4a16(ctypes.byref(odd_ff), *args[:5], fake_ws,
+                               moe.moe_workspace_size(odd_ff), None, None) == 2
+    # missing struct, missing / misaligned matrices, short workspace
+    assert L.moe_forward_w4a16(ctypes.byref(cfg), P(256), P(256), None, None, P(256), fake_ws,
+                               need, None, None) == 1
+    bad_q = _w4_layer(bad=("down", (264, 256)))
+    assert L.moe_forward_w4a16(ctypes.byref(cfg), P(256), P(256), None, ctypes.byref(bad_q),
+                               P(256), fake_ws, need, None, None) == 1
+    no_shared = _w4_layer(bad=("shared_up", (None, None)))
+    assert L.moe_forward_w4a16(ctypes.byref(cfg), P(256), P(256), None, ctypes.byref(no_shared),
+                               P(256), fake_ws, need, None, None) == 1
+    assert L.moe_forward_w4a16(ctypes.byref(cfg), *args[:5], fake_ws, need - 1, None, None) == 6
+    # the grouped step does not read the shared matrices
+    assert L.moe_grouped_ffn_w4a16(ctypes.byref(cfg), P(256), P(256), P(256), None,
+                                   ctypes.byref(no_shared), P(256), fake_ws, need - 1, None) == 6
+    assert L.moe_grouped_ffn_w4a16(ctypes.byref(f32), P(256), P(256), P(256), None,
+                                   ctypes.byref(st), P(256), fake_ws,
+                                   moe.moe_workspace_size(f32), None) == 2
+
+
+def test_w4_struct_layout_matches_c(tmp_path):
+    prog = tmp_path / "w4layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe.h"\n'
+                    "int main(){printf(\"%zu %zu %zu\\n\", sizeof(moe_w4), sizeof(moe_w4_layer),"
+                    " offsetof(moe_w4_layer, shared_down));return 0;}\n")
+    exe = tmp_path / "w4layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)], text=True).split()]
+    assert got == [ctypes.sizeof(moe.MoeW4), ctypes.sizeof(moe.MoeW4Layer),
+                   moe.MoeW4Layer.shared_down.offset]

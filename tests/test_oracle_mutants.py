@@ -20,7 +20,7 @@ MUTANTS = {
     "drop_shared_term": ("            acc[i] += y[i];\n    }\n    store_row(out_t",
                          "            acc[i] += 0.0 * y[i];\n    }\n    store_row(out_t"),
     "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
-    "down_transposed": ("elem(Wd, dtype, (int64_t)i * F + n)", "elem(Wd, dtype, (int64_t)n * d + i)"),
+    "down_transposed": ("wval(Wd, dtype, i, n, F)", "wval(Wd, dtype, n, i, d)"),
     "gate_up_swapped": ("double hv = silu(g) * u;", "double hv = silu(u) * g;"),
     "wrong_slot_weight": ("acc[i] += (double)w_t[j] * y[i];", "acc[i] += (double)w_t[0] * y[i];"),
     "ties_to_higher_index": ("if (!chosen[e] && (best < 0 || sel[e] > sel[best]))",
@@ -37,6 +37,14 @@ MUTANTS = {
     "selection_bias_ignored": ("sel[e] = (b_r && bias_mode == 2) ? (float)((double)probs[e] + (double)b_r[e]) : probs[e];",
                                "sel[e] = probs[e];"),
     "selection_bias_in_weights": ("ws += (double)probs[idx[j]];", "ws += (double)sel[idx[j]];"),
+    "w4_nibble_order": ("int nib = (col & 1) ? (byte >> 4) : (byte & 15);",
+                        "int nib = (col & 1) ? (byte & 15) : (byte >> 4);"),
+    "w4_unsigned_codes": ("int code = nib >= 8 ? nib - 16 : nib;", "int code = nib;"),
+    "w4_scale_over_8": ("float sc = mx / 7.0f;", "float sc = mx / 8.0f;"),
+    "w4_round_half_away": ("float t = nearbyintf(v / sc);", "float t = roundf(v / sc);"),
+    "w4_pack_swapped": ("if (col & 1)", "if (!(col & 1))"),
+    "w4_first_group_scale": ("m->s[(col / ORC_W4_GROUP) * m->rows + row]", "m->s[row]"),
+    "w4_scales_row_major": ("s[(int64_t)g * rows + r] = sc;", "s[r * groups + g] = sc;"),
     "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
 }
 
@@ -50,7 +58,7 @@ def _run_pins_against(source: str, tmp_path):
     env = dict(os.environ, MOE_ORACLE_LIB=str(so), OMP_NUM_THREADS="2")
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_route.py", "test_oracle_permute.py", "test_oracle_layer.py",
-              "test_oracle_stats.py")]
+              "test_oracle_stats.py", "test_oracle_w4.py")]
     return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                            *tests], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
 
