@@ -52,7 +52,8 @@ def lib():
         P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
         L.oracle_round_bf16.argtypes = [D]
         L.oracle_round_bf16.restype = ctypes.c_uint16
-        L.oracle_route.argtypes = [I64, I32, I32, I32, I32, P, P, P, I32, I32, P, P, P, P]
+        L.oracle_route.argtypes = [I64, I32, I32, I32, I32, P, P, P, I32, I32, P, P, P, P, P]
+        L.oracle_router_stats.argtypes = [I64, I32, I32, P, P, P, P, P, P]
         L.oracle_capacity.argtypes = [I64, I32, I32, D]
         L.oracle_capacity.restype = I64
         L.oracle_permute.argtypes = [I64, I32, I32, P, I64, P, P, P, P, P, P]
@@ -70,7 +71,7 @@ def lib():
         L.oracle_forward_grouped.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
                                              P, P, P, I32, P, P, P, P, P, P, P]
         L.oracle_stats.argtypes = [I64, I32, I32, P, P, P, P, D, P, P, P, P]
-        for fn in ("oracle_route", "oracle_permute", "oracle_moe_token", "oracle_moe_token_w",
+        for fn in ("oracle_route", "oracle_router_stats", "oracle_permute", "oracle_moe_token", "oracle_moe_token_w",
                    "oracle_quantize_w4", "oracle_forward_naive",
                    "oracle_forward_grouped", "oracle_stats"):
             getattr(L, fn).restype = I32
@@ -115,8 +116,10 @@ def capacity(N: int, k: int, E: int, cf: float) -> int:
 
 # ---------------------------------------------------------------- steps
 
-def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1, bias_mode: Optional[int] = None):
-    """Router: returns idx [N,k] int32, w [N,k] f32, probs [N,E] f32, gap [N] f32.
+def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1, bias_mode: Optional[int] = None,
+          with_lse: bool = False):
+    """Router: returns idx [N,k] int32, w [N,k] f32, probs [N,E] f32, gap [N] f32 (and, with
+    with_lse, lse [N] f64: log-sum-exp of each token's raw logits).
     bias_mode: 1 = b_r added to the logits (default when b_r is given), 2 = b_r added to the
     probabilities for the top-k choice only."""
     bias_mode = (0 if b_r is None else 1) if bias_mode is None else bias_mode
@@ -129,11 +132,27 @@ def route(x, W_r, b_r, k: int, dtype: int, renorm: int = 1, bias_mode: Optional[
     w = np.zeros((N, k), np.float32)
     probs = np.zeros((N, E), np.float32)
     gap = np.zeros((N,), np.float32)
+    lse = np.zeros((N,), np.float64) if with_lse else None
     rc = lib().oracle_route(N, d, E, k, dtype, _p(x), _p(W_r), _p(b), bias_mode, renorm,
-                            _p(idx), _p(w), _p(probs), _p(gap))
+                            _p(idx), _p(w), _p(probs), _p(gap), _p(lse))
     if rc:
         raise ValueError("oracle_route rejected its arguments")
-    return idx, w, probs, gap
+    return (idx, w, probs, gap, lse) if with_lse else (idx, w, probs, gap)
+
+
+def router_stats(idx: np.ndarray, w: np.ndarray, lse: np.ndarray, E: int):
+    """z-loss, per-expert importance and its CV^2 (see oracle_router_stats)."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    N, k = idx.shape
+    z = ctypes.c_double(0)
+    cv2 = ctypes.c_double(0)
+    imp = np.zeros(E, np.float64)
+    if lib().oracle_router_stats(N, E, k, _p(idx), _p(w), _p(lse), ctypes.byref(z), _p(imp),
+                                 ctypes.byref(cv2)):
+        raise ValueError("oracle_router_stats rejected its arguments")
+    return dict(z_loss=z.value, importance=imp, importance_cv2=cv2.value)
 
 
 def permute(idx: np.ndarray, E: int, cap: int = -1):

@@ -119,7 +119,7 @@ static double wval(const void *p, int wdtype, int64_t row, int64_t col, int64_t 
 /* For one token: probs[E] (fp32), idx[k], w[k], gap.  Returns 0. */
 static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t,
                         const float *W_r, const float *b_r, int bias_mode, int renorm,
-                        float *probs, int32_t *idx, float *w, float *gap)
+                        float *probs, int32_t *idx, float *w, float *gap, double *lse)
 {
     float *logit = (float *)malloc(sizeof(float) * (size_t)E);
     float *sel = (float *)malloc(sizeof(float) * (size_t)E);
@@ -144,6 +144,9 @@ static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t
         s += exp((double)logit[e] - mx);
     for (int e = 0; e < E; e++)
         probs[e] = (float)(exp((double)logit[e] - mx) / s);
+    /* log-sum-exp of the raw logits (the z-loss term of "混合专家模型 (MoE)" section 三.3) */
+    if (lse)
+        *lse = mx + log(s);
 
     /* selection score: the probability, or with a selection-only bias ("混合专家 MoE",
      * 负载均衡: the bias only picks the top-k, it does not change the weights) p_e + b_e,
@@ -193,7 +196,7 @@ static void route_token(int d, int E, int k, int dtype, const void *x, int64_t t
  */
 int oracle_route(int64_t N, int d, int E, int k, int dtype, const void *x,
                  const float *W_r, const float *b_r, int bias_mode, int renorm,
-                 int32_t *idx, float *w, float *probs, float *gap)
+                 int32_t *idx, float *w, float *probs, float *gap, double *lse)
 {
     if (N < 0 || d <= 0 || E <= 0 || k <= 0 || k > E)
         return 1;
@@ -201,7 +204,8 @@ int oracle_route(int64_t N, int d, int E, int k, int dtype, const void *x,
     for (int64_t t = 0; t < N; t++) {
         float *p = (float *)malloc(sizeof(float) * (size_t)E);
         float g;
-        route_token(d, E, k, dtype, x, t, W_r, b_r, bias_mode, renorm, p, idx + t * k, w + t * k, &g);
+        route_token(d, E, k, dtype, x, t, W_r, b_r, bias_mode, renorm, p, idx + t * k, w + t * k, &g,
+                    lse ? lse + t : NULL);
         if (probs)
             memcpy(probs + t * (int64_t)E, p, sizeof(float) * (size_t)E);
         if (gap)
@@ -396,7 +400,8 @@ int oracle_forward_naive(int64_t N, int d, int F, int E, int k, int S, int Fs, i
     int32_t *idx = idx_o ? idx_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
     float *w = w_o ? w_o : (float *)malloc(sizeof(float) * (size_t)(A ? A : 1));
     int32_t *keep = keep_o ? keep_o : (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
-    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, probs_o, gap_o);
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, probs_o, gap_o,
+                          NULL);
     if (rc) {
         if (!idx_o) free(idx);
         if (!w_o) free(w);
@@ -457,7 +462,8 @@ int oracle_forward_grouped(int64_t N, int d, int F, int E, int k, int S, int Fs,
     double *acc = (double *)calloc((size_t)(N * d ? N * d : 1), sizeof(double));
     double *xt = (double *)malloc(sizeof(double) * (size_t)d);
     double *y = (double *)malloc(sizeof(double) * (size_t)d);
-    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, NULL, NULL);
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, NULL, NULL,
+                          NULL);
     if (!rc)
         rc = oracle_permute(N, k, E, idx, oracle_capacity(N, k, E, cf), counts, offsets, kept,
                             kept_off, perm, pos);
@@ -545,6 +551,44 @@ int oracle_stats(int64_t N, int E, int k, const int32_t *idx, const float *probs
         if (gap && (double)gap[t] < tie_eps)
             counters[2]++;
     }
+    return 0;
+}
+
+/* ---------- router statistics: z-loss and importance ("混合专家模型 (MoE)", 二.2 and 三.3) ---------- */
+
+/*
+ * oracle_router_stats, plain definitions (the pages' formulas are lost; the readings):
+ *   z_loss = (1/N) sum_t lse_t^2, lse_t = log sum_e exp(l_t,e) of the raw logits, before top-k;
+ *   imp[e] = sum_t sum_j w_t,j [idx_t,j == e]: the gate weight each expert was assigned (the
+ *            renormalised top-k weights), over every assignment before any capacity drop;
+ *   cv2    = Var(imp) / Mean(imp)^2 over the E experts, population variance (0 if the mean is 0).
+ * Returns 1 on bad sizes.
+ */
+int oracle_router_stats(int64_t N, int E, int k, const int32_t *idx, const float *w,
+                        const double *lse, double *z_loss, double *imp, double *cv2)
+{
+    if (N < 0 || E <= 0 || k <= 0)
+        return 1;
+    double z = 0.0;
+    for (int64_t t = 0; t < N; t++)
+        z += lse[t] * lse[t];
+    *z_loss = N > 0 ? z / (double)N : 0.0;
+    for (int e = 0; e < E; e++)
+        imp[e] = 0.0;
+    for (int64_t f = 0; f < N * (int64_t)k; f++) {
+        if (idx[f] < 0 || idx[f] >= E)
+            return 1;
+        imp[idx[f]] += (double)w[f];
+    }
+    double mean = 0.0;
+    for (int e = 0; e < E; e++)
+        mean += imp[e];
+    mean /= (double)E;
+    double var = 0.0;
+    for (int e = 0; e < E; e++)
+        var += (imp[e] - mean) * (imp[e] - mean);
+    var /= (double)E;
+    *cv2 = mean > 0.0 ? var / (mean * mean) : 0.0;
     return 0;
 }
 

@@ -45,6 +45,10 @@ MUTANTS = {
     "w4_pack_swapped": ("if (col & 1)", "if (!(col & 1))"),
     "w4_first_group_scale": ("m->s[(col / ORC_W4_GROUP) * m->rows + row]", "m->s[row]"),
     "w4_scales_row_major": ("s[(int64_t)g * rows + r] = sc;", "s[r * groups + g] = sc;"),
+    "z_mean_of_lse": ("z += lse[t] * lse[t];", "z += lse[t];"),
+    "importance_counts": ("imp[idx[f]] += (double)w[f];", "imp[idx[f]] += 1.0;"),
+    "cv2_sample_variance": ("    var /= (double)E;", "    var /= (double)(E - 1);"),
+    "lse_without_max": ("*lse = mx + log(s);", "*lse = log(s);"),
     "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
 }
 
@@ -58,7 +62,7 @@ def _run_pins_against(source: str, tmp_path):
     env = dict(os.environ, MOE_ORACLE_LIB=str(so), OMP_NUM_THREADS="2")
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_route.py", "test_oracle_permute.py", "test_oracle_layer.py",
-              "test_oracle_stats.py", "test_oracle_w4.py")]
+              "test_oracle_stats.py", "test_oracle_w4.py", "test_oracle_router_stats.py")]
     return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                            *tests], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
 
