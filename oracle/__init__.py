@@ -70,8 +70,11 @@ def lib():
                                            P, P, P, I32, P, P, P, P, P, P, P, P, P, P, P, P]
         L.oracle_forward_grouped.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
                                              P, P, P, I32, P, P, P, P, P, P, P]
+        L.oracle_backward.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, D, I32, I32,
+                                      P, P, P, I32, P, P, P, P, P, P, P, D, D,
+                                      P, P, P, P, P, P, P, P, P]
         L.oracle_stats.argtypes = [I64, I32, I32, P, P, P, P, D, P, P, P, P]
-        for fn in ("oracle_route", "oracle_router_stats", "oracle_permute", "oracle_moe_token", "oracle_moe_token_w",
+        for fn in ("oracle_route", "oracle_router_stats", "oracle_backward", "oracle_permute", "oracle_moe_token", "oracle_moe_token_w",
                    "oracle_quantize_w4", "oracle_forward_naive",
                    "oracle_forward_grouped", "oracle_stats"):
             getattr(L, fn).restype = I32
@@ -296,6 +299,37 @@ def forward_naive(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int 
     if rc:
         raise ValueError("oracle_forward_naive rejected its arguments")
     return out, dict(idx=idx, w=w, keep=keep, probs=probs, gap=gap)
+
+
+def backward(layer: dict, k: int, dtype: int, dout, cf: float = 0.0, renorm: int = 1,
+             round_h: Optional[int] = None, bias_mode: Optional[int] = None,
+             aux_coef: float = 0.0, z_coef: float = 0.0) -> dict:
+    """Gradients of sum <dout, out> + aux_coef L_aux + z_coef L_z (see oracle_backward), fp64:
+    dx [N,d], dW_r [E,d], db [E], dW_gate, dW_up [E,F,d], dW_down [E,d,F] and the shared
+    dWs_gate, dWs_up [S,F_s,d], dWs_down [S,d,F_s] (None without shared experts)."""
+    x, W_r, b_r, Wg, Wu, Wd, Wsg, Wsu, Wsd = _layer_arrays(layer, dtype)
+    bias_mode = (0 if b_r is None else 1) if bias_mode is None else bias_mode
+    round_h = (1 if dtype == BF16 else 0) if round_h is None else round_h
+    N, d = x.shape
+    E, F = Wg.shape[0], Wg.shape[1]
+    S = 0 if Wsg is None else Wsg.shape[0]
+    Fs = 0 if Wsg is None else Wsg.shape[1]
+    dout = np.ascontiguousarray(np.asarray(dout, np.float64).reshape(N, d))
+    z = lambda *shape: np.zeros(shape, np.float64)
+    g = dict(dx=z(N, d), dW_r=z(E, d), db=z(E), dW_gate=z(E, F, d), dW_up=z(E, F, d),
+             dW_down=z(E, d, F), dWs_gate=z(max(S, 1), Fs, d), dWs_up=z(max(S, 1), Fs, d),
+             dWs_down=z(max(S, 1), d, Fs))
+    rc = lib().oracle_backward(N, d, F, E, k, S, Fs, dtype, float(cf), renorm, round_h, _p(x),
+                               _p(W_r), _p(b_r), bias_mode, _p(Wg), _p(Wu), _p(Wd), _p(Wsg),
+                               _p(Wsu), _p(Wsd), _p(dout), float(aux_coef), float(z_coef),
+                               _p(g["dx"]), _p(g["dW_r"]), _p(g["db"]), _p(g["dW_gate"]),
+                               _p(g["dW_up"]), _p(g["dW_down"]), _p(g["dWs_gate"]),
+                               _p(g["dWs_up"]), _p(g["dWs_down"]))
+    if rc:
+        raise ValueError("oracle_backward rejected its arguments")
+    if S == 0:
+        g["dWs_gate"] = g["dWs_up"] = g["dWs_down"] = None
+    return g
 
 
 def forward_grouped(layer: dict, k: int, dtype: int, cf: float = 0.0, renorm: int = 1,

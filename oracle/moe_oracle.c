@@ -554,6 +554,181 @@ int oracle_stats(int64_t N, int E, int k, const int32_t *idx, const float *probs
     return 0;
 }
 
+/* ---------- backward pass (chain rule through the forward above) ---------- */
+
+/*
+ * One SwiGLU expert's backward for one token: the forward h = silu(W_g x) * (W_u x) (rounded to
+ * bf16 when round_h, the forward's rounding point, whose derivative is taken as 1),
+ * y = W_d h; the upstream gradient of y is wgt * dout.  Accumulates dW_g += dg x^T,
+ * dW_u += du x^T, dW_d += dy h^T and dx += W_g^T dg + W_u^T du; returns <dout, y>.
+ */
+static double swiglu_backward(const double *xt, int d, int F, int wdtype, const void *Wg,
+                              const void *Wu, const void *Wd, int round_h, double wgt,
+                              const double *dout, double *dx, double *dWg, double *dWu,
+                              double *dWd)
+{
+    double *g = (double *)malloc(sizeof(double) * (size_t)F);
+    double *u = (double *)malloc(sizeof(double) * (size_t)F);
+    double *h = (double *)malloc(sizeof(double) * (size_t)F);
+    double *dh = (double *)malloc(sizeof(double) * (size_t)F);
+    for (int n = 0; n < F; n++) {
+        double gv = 0.0, uv = 0.0;
+        for (int i = 0; i < d; i++) {
+            gv += wval(Wg, wdtype, n, i, d) * xt[i];
+            uv += wval(Wu, wdtype, n, i, d) * xt[i];
+        }
+        g[n] = gv;
+        u[n] = uv;
+        double hv = silu(gv) * uv;
+        h[n] = round_h ? round_to_bf16_value(hv) : hv;
+    }
+    /* y = W_d h, <dout, y>, dh = W_d^T dy, dW_d += dy h^T with dy = wgt * dout */
+    double dot = 0.0;
+    for (int n = 0; n < F; n++)
+        dh[n] = 0.0;
+    for (int i = 0; i < d; i++) {
+        double y = 0.0;
+        for (int n = 0; n < F; n++)
+            y += wval(Wd, wdtype, i, n, F) * h[n];
+        dot += dout[i] * y;
+        double dy = wgt * dout[i];
+        for (int n = 0; n < F; n++) {
+            dh[n] += wval(Wd, wdtype, i, n, F) * dy;
+            dWd[(int64_t)i * F + n] += dy * h[n];
+        }
+    }
+    /* h = silu(g) u: dg = dh u silu'(g), du = dh silu(g); silu'(z) = s (1 + z (1 - s)) */
+    for (int n = 0; n < F; n++) {
+        double sg = 1.0 / (1.0 + exp(-g[n]));
+        double dg = dh[n] * u[n] * sg * (1.0 + g[n] * (1.0 - sg));
+        double du = dh[n] * g[n] * sg;
+        for (int i = 0; i < d; i++) {
+            dWg[(int64_t)n * d + i] += dg * xt[i];
+            dWu[(int64_t)n * d + i] += du * xt[i];
+            dx[i] += wval(Wg, wdtype, n, i, d) * dg + wval(Wu, wdtype, n, i, d) * du;
+        }
+    }
+    free(g);
+    free(u);
+    free(h);
+    free(dh);
+    return dot;
+}
+
+/*
+ * oracle_backward: gradients of
+ *     L = sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z
+ * with respect to x, W_r, b_r (bias_mode 1), the routed and the shared expert weights, where
+ * out is the layer of oracle_forward_naive, L_aux = E sum_e f_e P_e ("混合专家 MoE", 负载均衡)
+ * and L_z = (1/N) sum_t lse_t^2 (oracle_router_stats).  Readings: the top-k choice and the
+ * capacity drop are piecewise constant (no gradient through the selection itself); f_e is a
+ * count (constant); the bf16 rounding of h passes the gradient unchanged; the selection-only
+ * bias (bias_mode 2) gets no gradient.  The routing weight w_j = p_ij / sum_sel p (renorm) so
+ * dp_ij = (dw_j - sum_j' w_j' dw_j') / sum_sel p, with dw_j = <dout_t, y_j> for kept slots;
+ * softmax: dl_e = p_e (dp_e - sum_e' p_e' dp_e'); the z-loss adds (2 z_coef / N) lse_t p_e.
+ * All outputs fp64, zeroed first; db may be NULL.  Sequential (deterministic).
+ */
+int oracle_backward(int64_t N, int d, int F, int E, int k, int S, int Fs, int dtype, double cf,
+                    int renorm, int round_h, const void *x, const float *W_r, const float *b_r,
+                    int bias_mode, const void *Wg, const void *Wu, const void *Wd,
+                    const void *Wsg, const void *Wsu, const void *Wsd, const double *dout,
+                    double aux_coef, double z_coef, double *dx, double *dW_r, double *db,
+                    double *dWg, double *dWu, double *dWd, double *dWsg, double *dWsu,
+                    double *dWsd)
+{
+    if (N < 0 || k > E || k <= 0 || k > 64 || S < 0 || S > 64 || d <= 0 || F <= 0)
+        return 1;
+    int64_t A = N * k;
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
+    float *w = (float *)malloc(sizeof(float) * (size_t)(A ? A : 1));
+    int32_t *keep = (int32_t *)malloc(sizeof(int32_t) * (size_t)(A ? A : 1));
+    float *probs = (float *)malloc(sizeof(float) * (size_t)(N ? N : 1) * (size_t)E);
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(N ? N : 1));
+    double *counts = (double *)calloc((size_t)E, sizeof(double));
+    int rc = oracle_route(N, d, E, k, dtype, x, W_r, b_r, bias_mode, renorm, idx, w, probs, NULL,
+                          lse);
+    if (!rc) {
+        oracle_keep_naive(N, k, E, idx, oracle_capacity(N, k, E, cf), keep);
+        for (int64_t f = 0; f < A; f++)
+            counts[idx[f]] += 1.0;
+        memset(dx, 0, sizeof(double) * (size_t)N * (size_t)d);
+        memset(dW_r, 0, sizeof(double) * (size_t)E * (size_t)d);
+        if (db)
+            memset(db, 0, sizeof(double) * (size_t)E);
+        memset(dWg, 0, sizeof(double) * (size_t)E * (size_t)F * (size_t)d);
+        memset(dWu, 0, sizeof(double) * (size_t)E * (size_t)F * (size_t)d);
+        memset(dWd, 0, sizeof(double) * (size_t)E * (size_t)d * (size_t)F);
+        if (S > 0) {
+            memset(dWsg, 0, sizeof(double) * (size_t)S * (size_t)Fs * (size_t)d);
+            memset(dWsu, 0, sizeof(double) * (size_t)S * (size_t)Fs * (size_t)d);
+            memset(dWsd, 0, sizeof(double) * (size_t)S * (size_t)d * (size_t)Fs);
+        }
+        double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)E);
+        double dw[64];
+        for (int64_t t = 0; t < N; t++) {
+            const double *dt = dout + t * (int64_t)d;
+            double *dxt = dx + t * (int64_t)d;
+            for (int i = 0; i < d; i++)
+                xt[i] = elem(x, dtype, t * (int64_t)d + i);
+            /* routed experts */
+            for (int j = 0; j < k; j++) {
+                dw[j] = 0.0;
+                if (!keep[t * k + j])
+                    continue;
+                int e = idx[t * k + j];
+                dw[j] = swiglu_backward(xt, d, F, dtype, expert_mat(Wg, dtype, e, F, d),
+                                        expert_mat(Wu, dtype, e, F, d),
+                                        expert_mat(Wd, dtype, e, d, F), round_h,
+                                        (double)w[t * k + j], dt, dxt,
+                                        dWg + (int64_t)e * F * d, dWu + (int64_t)e * F * d,
+                                        dWd + (int64_t)e * d * F);
+            }
+            /* shared experts, weight 1 */
+            for (int sh = 0; sh < S; sh++)
+                swiglu_backward(xt, d, Fs, dtype, expert_mat(Wsg, dtype, sh, Fs, d),
+                                expert_mat(Wsu, dtype, sh, Fs, d),
+                                expert_mat(Wsd, dtype, sh, d, Fs), round_h, 1.0, dt, dxt,
+                                dWsg + (int64_t)sh * Fs * d, dWsu + (int64_t)sh * Fs * d,
+                                dWsd + (int64_t)sh * d * Fs);
+            /* routing weights -> probabilities */
+            const float *pt = probs + t * (int64_t)E;
+            for (int e = 0; e < E; e++)
+                dp[e] = aux_coef * (double)E * (counts[e] / (double)A) / (double)N;
+            double ssel = 0.0, wdw = 0.0;
+            for (int j = 0; j < k; j++) {
+                ssel += (double)pt[idx[t * k + j]];
+                wdw += (double)w[t * k + j] * dw[j];
+            }
+            for (int j = 0; j < k; j++)
+                dp[idx[t * k + j]] += renorm ? (dw[j] - wdw) / ssel : dw[j];
+            /* softmax -> logits, plus the z-loss term */
+            double pdp = 0.0;
+            for (int e = 0; e < E; e++)
+                pdp += (double)pt[e] * dp[e];
+            for (int e = 0; e < E; e++) {
+                double dl = (double)pt[e] * (dp[e] - pdp) +
+                            2.0 * z_coef / (double)N * lse[t] * (double)pt[e];
+                for (int i = 0; i < d; i++) {
+                    dW_r[(int64_t)e * d + i] += dl * xt[i];
+                    dxt[i] += dl * (double)W_r[(int64_t)e * d + i];
+                }
+                if (db && b_r && bias_mode == 1)
+                    db[e] += dl;
+            }
+        }
+        free(xt);
+        free(dp);
+    }
+    free(idx);
+    free(w);
+    free(keep);
+    free(probs);
+    free(lse);
+    free(counts);
+    return rc;
+}
+
 /* ---------- router statistics: z-loss and importance ("混合专家模型 (MoE)", 二.2 and 三.3) ---------- */
 
 /*

@@ -49,6 +49,17 @@ MUTANTS = {
     "importance_counts": ("imp[idx[f]] += (double)w[f];", "imp[idx[f]] += 1.0;"),
     "cv2_sample_variance": ("    var /= (double)E;", "    var /= (double)(E - 1);"),
     "lse_without_max": ("*lse = mx + log(s);", "*lse = log(s);"),
+    "bwd_silu_derivative": ("sg * (1.0 + g[n] * (1.0 - sg))", "sg"),
+    "bwd_renorm_without_mean": ("(dw[j] - wdw) / ssel", "dw[j] / ssel"),
+    "bwd_softmax_without_mean": ("(double)pt[e] * (dp[e] - pdp)", "(double)pt[e] * dp[e]"),
+    "bwd_down_grad_transposed": ("dWd[(int64_t)i * F + n] += dy * h[n];",
+                                 "dWd[(int64_t)n * d + i] += dy * h[n];"),
+    "bwd_aux_without_E": ("aux_coef * (double)E * (counts[e] / (double)A) / (double)N",
+                          "aux_coef * (counts[e] / (double)A) / (double)N"),
+    "bwd_z_without_two": ("2.0 * z_coef / (double)N * lse[t]", "z_coef / (double)N * lse[t]"),
+    "bwd_no_router_dx": ("                    dxt[i] += dl * (double)W_r[(int64_t)e * d + i];\n",
+                         ""),
+    "bwd_dropped_slots_pass": ("                if (!keep[t * k + j])\n                    continue;\n", ""),
     "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
 }
 
@@ -62,7 +73,8 @@ def _run_pins_against(source: str, tmp_path):
     env = dict(os.environ, MOE_ORACLE_LIB=str(so), OMP_NUM_THREADS="2")
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_route.py", "test_oracle_permute.py", "test_oracle_layer.py",
-              "test_oracle_stats.py", "test_oracle_w4.py", "test_oracle_router_stats.py")]
+              "test_oracle_stats.py", "test_oracle_w4.py", "test_oracle_router_stats.py",
+              "test_oracle_backward.py")]
     return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                            *tests], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
 
