@@ -108,6 +108,7 @@ MOE_API int64_t moe_grouped_rows(const moe_cfg *cfg);
  *   P_sum [E] fp32 out: sum over tokens of p[t,e] (the load-balance P_e times N);
  *   gap [N] fp32 out, nullable: s_(k) - s_(k+1) of the selection scores s (= p, or p + b_r
  *   with bias_mode 2; +inf when k == E).
+ * Also writes each token's log-sum-exp of its logits into the workspace (moe_buffers.lse).
  */
 MOE_API moe_status moe_route(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
                      int32_t *idx, float *w, float *P_sum, float *gap,
@@ -220,6 +221,7 @@ typedef struct {
     float *row_weight;     /* [R] */
     void *x_perm;          /* [R,d] */
     void *y_perm;          /* [R,d] */
+    float *lse;            /* [N] log-sum-exp of each token's router logits (for the z-loss) */
 } moe_buffers;
 
 MOE_API moe_status moe_forward_buffers(const moe_cfg *cfg, void *ws, size_t ws_bytes, moe_buffers *out_host);
@@ -315,6 +317,29 @@ MOE_API moe_status moe_stats(const moe_cfg *cfg, const int32_t *counts, const in
  */
 MOE_API moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint32_t timeout_us,
                                              void *stream);
+
+/* Router statistics the pages name for training ("混合专家模型 (MoE)：大规模稀疏条件计算的架构与
+ * 工程实践": section 二.2 importance loss, section 三.3 z-loss; the formulas are lost there). */
+typedef struct {
+    double z_loss;             /* (1/N) sum_t lse_t^2, lse_t = log sum_e exp(logit_t,e) */
+    double importance_cv2;     /* Var(Imp) / Mean(Imp)^2 over experts (population variance) */
+    double importance_mean;    /* Mean(Imp) = sum of all routing weights / E */
+} moe_router_summary;
+
+/*
+ * moe_router_stats -- z-loss and importance of one routed batch.  Imp_e = sum of the routing
+ * weights w (renormalised top-k) of the assignments to expert e, counted before any capacity
+ * drop; the z-loss uses the raw logits before top-k (with the bias when bias_mode == 1, without
+ * the selection-only bias of bias_mode 2).  Both sums are deterministic (fixed order, fp64).
+ *   lse [N] fp32 (moe_forward_buffers().lse, written by moe_route / moe_forward);
+ *   w [N,k] fp32; perm [N*k], offsets [E+1] int32 (moe_permute);
+ *   importance_host [E] fp32 host out, nullable; summary_host host out.
+ * Synchronises the stream.
+ */
+MOE_API moe_status moe_router_stats(const moe_cfg *cfg, const float *lse, const float *w,
+                                    const int32_t *perm, const int32_t *offsets,
+                                    float *importance_host, moe_router_summary *summary_host,
+                                    void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronises the stream and reads the sticky device error word (MOE_DEVERR_* bits). */
 MOE_API moe_status moe_device_error(void *ws, size_t ws_bytes, int32_t *code_host, void *stream);

@@ -262,6 +262,43 @@ stats_final_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict
     }
 }
 
+// z-loss: block b sums lse^2 over its fixed token range in double (thread-strided, then a
+// fixed tree), so the partials and their order do not depend on timing.
+__global__ void __launch_bounds__(256)
+z_partial_kernel(const float* __restrict__ lse, int64_t N, double* __restrict__ z_part) {
+    __shared__ double sm[256];
+    const int64_t per = (N + gridDim.x - 1) / gridDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * per;
+    const int64_t t1 = t0 + per < N ? t0 + per : N;
+    double s = 0.0;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+        const double v = (double)lse[t];
+        s += v * v;
+    }
+    sm[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sm[threadIdx.x] += sm[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) z_part[blockIdx.x] = sm[0];
+}
+
+// importance: one warp per expert sums the weights of its segment of the expert-sorted slots
+// (lanes strided, fixed butterfly).
+__global__ void __launch_bounds__(256)
+importance_kernel(const float* __restrict__ w, const int32_t* __restrict__ perm,
+                  const int32_t* __restrict__ offsets, int E, double* __restrict__ imp) {
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (e >= E) return;
+    double s = 0.0;
+    for (int64_t i = offsets[e] + lane; i < offsets[e + 1]; i += 32) s += (double)w[perm[i]];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) imp[e] = s;
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* pos,
@@ -291,6 +328,15 @@ cudaError_t launch_plan_pairs(const int32_t* kept, const int32_t* kept_off, int 
                               int32_t* tail_off, cudaStream_t s) {
     plan_pairs_kernel<<<1, 1024, 0, s>>>(kept, kept_off, E, pair_off, tail_mtile, tail_rows, tail_off);
     return cudaGetLastError();
+}
+
+cudaError_t launch_router_stats(int64_t N, int E, int k, const float* lse, const float* w,
+                                const int32_t* perm, const int32_t* offsets, double* z_part,
+                                double* imp, cudaStream_t s) {
+    z_partial_kernel<<<kRouterStatBlocks, 256, 0, s>>>(lse, N, z_part);
+    importance_kernel<<<(E + 7) / 8, 256, 0, s>>>(w, perm, offsets, E, imp);
+    return cudaGetLastError();
+    (void)k;
 }
 
 cudaError_t launch_stats(const moe_cfg& c, const int32_t* counts, const int32_t* kept,

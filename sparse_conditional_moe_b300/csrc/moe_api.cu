@@ -73,6 +73,8 @@ WsLayout ws_layout(const moe_cfg& c) {
     L.idx = take(4 * (size_t)A);
     L.w = take(4 * (size_t)A);
     L.gap = take(4 * (size_t)N);
+    L.lse = take(4 * (size_t)N);
+    L.rstat = take(8 * (size_t)(kRouterStatBlocks + E));
     L.P_sum = take(4 * (size_t)E);
     L.counts = take(4 * (size_t)E);
     L.offsets = take(4 * (size_t)(E + 1));
@@ -387,7 +389,8 @@ moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const 
     MOE_TRY(need(P_sum, 4));
     if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
     const WsLayout L = ws_layout(*cfg);
-    MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.p_part), P_sum,
+    MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.lse),
+                           at<float>(ws, L.p_part), P_sum,
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits),
                            at<int32_t>(ws, L.err), (cudaStream_t)stream));
     return MOE_OK;
@@ -475,7 +478,8 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
-                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum),
+                           at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
+                           at<float>(ws, L.P_sum),
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
@@ -551,7 +555,8 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
-                           at<float>(ws, L.gap), at<float>(ws, L.p_part), at<float>(ws, L.P_sum),
+                           at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
+                           at<float>(ws, L.P_sum),
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
@@ -589,6 +594,53 @@ moe_status moe_forward_buffers(const moe_cfg* cfg, void* ws, size_t ws_bytes, mo
     out->row_weight = at<float>(ws, L.row_weight);
     out->x_perm = at<void>(ws, L.x_perm);
     out->y_perm = at<void>(ws, L.y_perm);
+    out->lse = at<float>(ws, L.lse);
+    return MOE_OK;
+}
+
+moe_status moe_router_stats(const moe_cfg* cfg, const float* lse, const float* w,
+                            const int32_t* perm, const int32_t* offsets, float* importance_host,
+                            moe_router_summary* summary, void* ws, size_t ws_bytes,
+                            void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (!summary) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(need(offsets, 4));
+    if (cfg->N > 0) {
+        MOE_TRY(need(lse, 4));
+        MOE_TRY(need(w, 4));
+        MOE_TRY(need(perm, 4));
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(*cfg);
+    double* zp = at<double>(ws, L.rstat);
+    double* imp = zp + kRouterStatBlocks;
+    MOE_CUDA(launch_router_stats(cfg->N, cfg->E, cfg->k, lse, w, perm, offsets, zp, imp, s));
+    const int E = cfg->E;
+    double* h = static_cast<double*>(malloc(sizeof(double) * (size_t)(kRouterStatBlocks + E)));
+    if (!h) return MOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(h, zp, sizeof(double) * (size_t)(kRouterStatBlocks + E),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        free(h);
+        return MOE_ERR_CUDA;
+    }
+    double z = 0.0, mean = 0.0, var = 0.0;
+    for (int b = 0; b < kRouterStatBlocks; b++) z += h[b];
+    for (int i = 0; i < E; i++) mean += h[kRouterStatBlocks + i];
+    mean /= (double)E;
+    for (int i = 0; i < E; i++) {
+        const double dv = h[kRouterStatBlocks + i] - mean;
+        var += dv * dv;
+    }
+    var /= (double)E;
+    summary->z_loss = cfg->N > 0 ? z / (double)cfg->N : 0.0;
+    summary->importance_mean = mean;
+    summary->importance_cv2 = mean > 0.0 ? var / (mean * mean) : 0.0;
+    if (importance_host)
+        for (int i = 0; i < E; i++) importance_host[i] = (float)h[kRouterStatBlocks + i];
+    free(h);
     return MOE_OK;
 }
 

@@ -36,7 +36,8 @@ struct WsLayout {
     size_t mtile_off;    // int32 [E + 1]: m-tile (or m-pair) prefix of the routed grouped GEMMs
     size_t tail_plan;    // int32 [3E + 1]: tail m-tile prefix, tail rows, tail row offsets
     size_t stats_f;      // float [2E + 8]: f, P, scalars
-    size_t idx, w, gap, P_sum, counts, offsets, kept, kept_offsets, perm, pos;
+    size_t idx, w, gap, lse, P_sum, counts, offsets, kept, kept_offsets, perm, pos;
+    size_t rstat;        // double [kRouterStatBlocks + E]: z-loss partials, importance
     size_t row_token, row_weight;
     size_t x_perm, h_perm, y_perm;   // [R, d], [R, F], [R, d]
     size_t h_sh, y_sh;               // [S, N, F_s], [S, N, d]
@@ -50,9 +51,11 @@ WsLayout ws_layout(const moe_cfg& c);
 // ------------------------------------------------------------------ launches
 // All return cudaGetLastError() of their launches.
 
+// lse [N] (nullable): log-sum-exp of each token's logits, for the z-loss.
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
-                          int32_t* idx, float* w, float* gap, float* p_part, float* P_sum,
-                          __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s);
+                          int32_t* idx, float* w, float* gap, float* lse, float* p_part,
+                          float* P_sum, __nv_bfloat16* w3, float* logits, int32_t* err,
+                          cudaStream_t s);
 
 // Tensor-core router logits [N, E] (fp32) for bf16 x (see router_tc.cu).
 cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
@@ -138,6 +141,13 @@ cudaError_t w4_down(const W4Group& g, const __nv_bfloat16* H, int F, const W4Mat
 
 cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* pos,
                            const void* y_sh, void* out, int32_t* err, cudaStream_t s);
+
+// Router statistics (z-loss partial sums over fixed token blocks, importance per expert
+// summed along the expert-sorted permutation), both deterministic, in double.
+constexpr int kRouterStatBlocks = 256;
+cudaError_t launch_router_stats(int64_t N, int E, int k, const float* lse, const float* w,
+                                const int32_t* perm, const int32_t* offsets, double* z_part,
+                                double* imp, cudaStream_t s);
 
 cudaError_t launch_stats(const moe_cfg& c, const int32_t* counts, const int32_t* kept,
                          const float* P_sum, const int32_t* pos, const float* gap,

@@ -26,7 +26,7 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_
            "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
            "moe_selftest_wait_timeout", "moe_status_string", "moe_quantize_w4",
-           "moe_grouped_ffn_w4a16", "moe_forward_w4a16")
+           "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats")
 MOE_W4_GROUP = 128
 
 
@@ -47,7 +47,12 @@ class MoeCfg(ctypes.Structure):
 class MoeBuffers(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("idx", "w", "gap", "P_sum", "counts", "offsets", "kept", "kept_offsets", "perm",
-                 "pos", "row_token", "row_weight", "x_perm", "y_perm")]
+                 "pos", "row_token", "row_weight", "x_perm", "y_perm", "lse")]
+
+
+class MoeRouterSummary(ctypes.Structure):
+    _fields_ = [("z_loss", ctypes.c_double), ("importance_cv2", ctypes.c_double),
+                ("importance_mean", ctypes.c_double)]
 
 
 class MoeStatsSummary(ctypes.Structure):
@@ -95,6 +100,7 @@ def lib():
             "moe_quantize_w4": [P, I64, ctypes.c_int32, P, P, P],
             "moe_grouped_ffn_w4a16": [C, P, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P],
             "moe_forward_w4a16": [C, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P, P],
+            "moe_router_stats": [C, P, P, P, P, P, ctypes.POINTER(MoeRouterSummary), P, SZ, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -308,6 +314,7 @@ def moe_forward_buffers(cfg, ws) -> dict:
         row_weight=view(b.row_weight, R, torch.float32, 4),
         x_perm=view(b.x_perm, R * d, act, esz).view(R, d),
         y_perm=view(b.y_perm, R * d, act, esz).view(R, d),
+        lse=view(b.lse, N, torch.float32, 4),
     )
 
 
@@ -323,6 +330,17 @@ def moe_stats(cfg, counts, kept, P_sum, pos, gap, ws, stream=None):
     return dict(f=list(f), P=list(P), aux=s.aux, dropped=s.dropped, fully_dropped=s.fully_dropped,
                 near_tie=s.near_tie, touched_experts=s.touched_experts, kept_rows=s.kept_rows,
                 device_error=s.device_error)
+
+
+def moe_router_stats(cfg, lse, w, perm, offsets, ws, stream=None) -> dict:
+    """z-loss, per-expert importance and its CV^2 (see include/moe.h).  Synchronises."""
+    imp = (ctypes.c_float * cfg.E)()
+    s = MoeRouterSummary()
+    _check(lib().moe_router_stats(ctypes.byref(cfg), _p(lse), _p(w), _p(perm), _p(offsets), imp,
+                                  ctypes.byref(s), _p(ws), ws.numel(), _s(stream)),
+           "moe_router_stats")
+    return dict(z_loss=s.z_loss, importance_cv2=s.importance_cv2,
+                importance_mean=s.importance_mean, importance=list(imp))
 
 
 def moe_selftest_wait_timeout(ws, timeout_us: int, stream=None):
@@ -372,6 +390,11 @@ class MoELayer:
         b = self.buffers()
         return moe_stats(self.cfg, b["counts"], b["kept"], b["P_sum"], b["pos"], b["gap"],
                          self.ws, stream)
+
+    def router_stats(self, stream=None) -> dict:
+        b = self.buffers()
+        return moe_router_stats(self.cfg, b["lse"], b["w"], b["perm"], b["offsets"], self.ws,
+                                stream)
 
     def device_error(self, stream=None) -> int:
         return moe_device_error(self.ws, stream)

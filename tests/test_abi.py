@@ -173,10 +173,28 @@ def test_w4a16_calls_validate_without_launching(L):
 def test_w4_struct_layout_matches_c(tmp_path):
     prog = tmp_path / "w4layout.c"
     prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe.h"\n'
-                    "int main(){printf(\"%zu %zu %zu\\n\", sizeof(moe_w4), sizeof(moe_w4_layer),"
-                    " offsetof(moe_w4_layer, shared_down));return 0;}\n")
+                    "int main(){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(moe_w4), sizeof(moe_w4_layer),"
+                    " offsetof(moe_w4_layer, shared_down), sizeof(moe_router_summary),"
+                    " offsetof(moe_buffers, lse));return 0;}\n")
     exe = tmp_path / "w4layout"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)])
     got = [int(v) for v in subprocess.check_output([str(exe)], text=True).split()]
     assert got == [ctypes.sizeof(moe.MoeW4), ctypes.sizeof(moe.MoeW4Layer),
-                   moe.MoeW4Layer.shared_down.offset]
+                   moe.MoeW4Layer.shared_down.offset, ctypes.sizeof(moe.MoeRouterSummary),
+                   moe.MoeBuffers.lse.offset]
+
+
+def test_router_stats_validate_without_launching(L):
+    P = ctypes.c_void_p
+    cfg = _cfg()
+    need = moe.moe_workspace_size(cfg)
+    fake_ws = P(1 << 20)
+    summ = moe.MoeRouterSummary()
+    assert L.moe_router_stats(ctypes.byref(cfg), P(256), P(256), P(256), P(256), None, None,
+                              fake_ws, need, None) == 1                       # no summary
+    assert L.moe_router_stats(ctypes.byref(cfg), P(256), P(256), P(256), P(256), None,
+                              ctypes.byref(summ), fake_ws, need - 1, None) == 6
+    assert L.moe_router_stats(ctypes.byref(cfg), None, P(256), P(256), P(256), None,
+                              ctypes.byref(summ), fake_ws, need, None) == 1   # no lse
+    assert L.moe_router_stats(ctypes.byref(cfg), P(256), P(256), P(256), P(258), None,
+                              ctypes.byref(summ), fake_ws, need, None) == 1   # misaligned offsets
