@@ -341,6 +341,17 @@ MOE_API moe_status moe_router_stats(const moe_cfg *cfg, const float *lse, const 
                                     float *importance_host, moe_router_summary *summary_host,
                                     void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * moe_selftest_gemm -- check of the backward pass's tcgen05 GEMM engine (the pages have no
+ * counterpart): C [M,N] fp32 = sum_k A(m,k) B(n,k) for one group, with A stored [M,K] (a_mn 0,
+ * K-major) or [K,M] (a_mn 1, M-major) and B stored [N,K] (b_mn 0) or [K,N] (b_mn 1), bf16.
+ * The K-contiguous or MN-contiguous dimension must be a multiple of 8, N of 4.  Uses 512 bytes
+ * of ws (the error word and a plan).  Asynchronous.
+ */
+MOE_API moe_status moe_selftest_gemm(int32_t a_mn, int32_t b_mn, int32_t M, int32_t N, int32_t K,
+                                     const void *A, const void *B, float *C, void *ws,
+                                     size_t ws_bytes, void *stream);
+
 /* Synchronises the stream and reads the sticky device error word (MOE_DEVERR_* bits). */
 MOE_API moe_status moe_device_error(void *ws, size_t ws_bytes, int32_t *code_host, void *stream);
 

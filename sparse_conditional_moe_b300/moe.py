@@ -26,7 +26,8 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_
            "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
            "moe_selftest_wait_timeout", "moe_status_string", "moe_quantize_w4",
-           "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats")
+           "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats",
+           "moe_selftest_gemm")
 MOE_W4_GROUP = 128
 
 
@@ -101,6 +102,7 @@ def lib():
             "moe_grouped_ffn_w4a16": [C, P, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P],
             "moe_forward_w4a16": [C, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P, P],
             "moe_router_stats": [C, P, P, P, P, P, ctypes.POINTER(MoeRouterSummary), P, SZ, P],
+            "moe_selftest_gemm": [ctypes.c_int32] * 5 + [P, P, P, P, SZ, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -341,6 +343,14 @@ def moe_router_stats(cfg, lse, w, perm, offsets, ws, stream=None) -> dict:
            "moe_router_stats")
     return dict(z_loss=s.z_loss, importance_cv2=s.importance_cv2,
                 importance_mean=s.importance_mean, importance=list(imp))
+
+
+def moe_selftest_gemm(A, B, M: int, N: int, K: int, a_mn: bool, b_mn: bool, ws, stream=None):
+    """C [M,N] fp32 = sum_k A(m,k) B(n,k) through the backward GEMM engine (see include/moe.h)."""
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check(lib().moe_selftest_gemm(int(a_mn), int(b_mn), M, N, K, _p(A), _p(B), _p(C), _p(ws),
+                                   ws.numel(), _s(stream)), "moe_selftest_gemm")
+    return C
 
 
 def moe_selftest_wait_timeout(ws, timeout_us: int, stream=None):
