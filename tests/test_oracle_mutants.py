@@ -60,7 +60,8 @@ MUTANTS = {
     "bwd_no_router_dx": ("                    dxt[i] += dl * (double)W_r[(int64_t)e * d + i];\n",
                          ""),
     "bwd_dropped_slots_pass": ("                if (!keep[t * k + j])\n                    continue;\n", ""),
-    "logit_transposed": ("(double)W_r[(int64_t)e * d + i]", "(double)W_r[(int64_t)i * E + e]"),
+    "logit_transposed": ("(int64_t)d + i) * (double)W_r[(int64_t)e * d + i]",
+                         "(int64_t)d + i) * (double)W_r[(int64_t)i * E + e]"),
 }
 
 
