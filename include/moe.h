@@ -284,6 +284,36 @@ MOE_API moe_status moe_forward_w4a16(const moe_cfg *cfg, const void *x, const fl
                                      void *ws, size_t ws_bytes, void *stream,
                                      void *const *events);
 
+/* ------------------------------------------------------------------ backward pass */
+
+/*
+ * moe_backward -- gradients of
+ *     L = sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z
+ * for the layer moe_forward just computed, by the chain rule through page "混合专家 MoE"
+ * (实现: MoE.route, Expert.forward; 负载均衡: aux_loss = E sum f_e P_e) and the z-loss of
+ * "混合专家模型 (MoE)" section 三.3 (L_z = mean_t lse_t^2, see moe_router_stats).  Readings: the
+ * top-k choice and capacity drops carry no gradient (piecewise constant); f_e is a count; the
+ * selection-only bias (bias_mode 2) gets none (db = 0); the bf16 rounding of h passes the
+ * gradient.  The routing weight w_j = p_ij / sum_sel p gives dp_ij = (dw_j - sum w dw) / sum_sel
+ * p with dw_j = <dout_t, y_j>; softmax backward; dW_r = dl^T x, db = sum_t dl (bias_mode 1).
+ *   Inputs as for moe_forward (the same pointers), dout [N,d] bf16.
+ *   ws: the forward's workspace, unchanged since that moe_forward (the router is rerun, bit
+ *   for bit, to get the probabilities); bws: moe_backward_workspace_size() bytes, 256-aligned.
+ *   Outputs fp32, overwritten: dx [N,d]; dW_r [E,d]; db [E] (nullable); dW_gate, dW_up [E,F,d];
+ *   dW_down [E,d,F]; dWs_gate, dWs_up [S,F_s,d], dWs_down [S,d,F_s] (ignored when S = 0).
+ * bf16 layers only, with d a multiple of 64 and d_ff, d_ff_shared multiples of 128 (else
+ * MOE_ERR_UNSUPPORTED).  Asynchronous; deterministic (no floating-point atomics).
+ */
+MOE_API moe_status moe_backward_workspace_size(const moe_cfg *cfg, size_t *bytes_host);
+MOE_API moe_status moe_backward(const moe_cfg *cfg, const void *x, const float *W_r,
+                                const float *b_r, const void *W_gate, const void *W_up,
+                                const void *W_down, const void *Ws_gate, const void *Ws_up,
+                                const void *Ws_down, const void *dout, double aux_coef,
+                                double z_coef, float *dx, float *dW_r, float *db, float *dW_gate,
+                                float *dW_up, float *dW_down, float *dWs_gate, float *dWs_up,
+                                float *dWs_down, void *ws, size_t ws_bytes, void *bws,
+                                size_t bws_bytes, void *stream);
+
 /* ------------------------------------------------------------------ statistics */
 
 /* Load-balance statistics ("混合专家 MoE", 负载均衡 section, aux_loss). */

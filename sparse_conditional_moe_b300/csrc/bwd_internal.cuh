@@ -48,4 +48,36 @@ cudaError_t tb_selftest(bool a_mn, bool b_mn, int M, int N, int K, const __nv_bf
                         const __nv_bfloat16* B, float* C, const int32_t* plan, int32_t* err,
                         cudaStream_t s);
 
+// ------------------------------------------------------------------ the backward pass (bwd.cu)
+
+struct BwdLayout {   // byte offsets in the backward workspace (256-byte aligned regions)
+    size_t probs, dl, dx_r, dw_row, c_off, s_plan;
+    size_t dout_pad, x_pad, dh, dgu, hw, dX, dw_part;
+    size_t dout_s, x_s, dh_s, dgu_s, hw_s, dX_s, dw_part_s;
+    size_t total;
+};
+BwdLayout bwd_layout(const moe_cfg& c);
+int64_t bwd_padded_rows(const moe_cfg& c);   // bound on the routed rows in padded segments
+int64_t bwd_shared_rows(const moe_cfg& c);   // N rounded up to 128
+
+struct BwdArgs {
+    const moe_cfg* cfg;
+    // forward inputs
+    const void* x;
+    const float* W_r;
+    const float* b_r;
+    const __nv_bfloat16 *Wg, *Wu, *Wd, *Wsg, *Wsu, *Wsd;
+    const __nv_bfloat16* dout;
+    double aux_coef, z_coef;
+    // outputs (fp32)
+    float *dx, *dW_r, *db, *dWg, *dWu, *dWd, *dWsg, *dWsu, *dWsd;
+    // the forward's workspace state
+    int32_t *idx, *pos, *counts, *kept, *kept_off, *row_token, *err;
+    float *w, *gap, *lse, *p_part, *P_sum, *row_weight, *logits;
+    __nv_bfloat16* w3;
+    const __nv_bfloat16 *x_perm, *h_perm, *h_sh;
+    void* bws;
+};
+cudaError_t run_backward(const BwdArgs& a, cudaStream_t s);
+
 }  // namespace moe

@@ -4,7 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "moe_internal.cuh"
+#include "bwd_internal.cuh"
 
 namespace moe {
 
@@ -572,6 +572,99 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
                               at<void>(ws, L.y_perm), ws, s, ev));
     MOE_TRY(do_shared_w4_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, *W,
                                      out, ws, s, ev));
+    return MOE_OK;
+}
+
+moe_status check_bwd_cfg(const moe_cfg* c) {
+    if (c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->d % 64 || c->d_ff % 128 || (c->n_shared > 0 && c->d_ff_shared % 128))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status moe_backward_workspace_size(const moe_cfg* cfg, size_t* bytes) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_bwd_cfg(cfg));
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = bwd_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_backward(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
+                        const void* W_gate, const void* W_up, const void* W_down,
+                        const void* Ws_gate, const void* Ws_up, const void* Ws_down,
+                        const void* dout, double aux_coef, double z_coef, float* dx, float* dW_r,
+                        float* db, float* dW_gate, float* dW_up, float* dW_down, float* dWs_gate,
+                        float* dWs_up, float* dWs_down, void* ws, size_t ws_bytes, void* bws,
+                        size_t bws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_bwd_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (!bws || !aligned(bws, 256) || bws_bytes < bwd_layout(*cfg).total) return MOE_ERR_WORKSPACE;
+    if (isnan(aux_coef) || isnan(z_coef)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(need(W_r, 16));
+    if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
+    MOE_TRY(check_weights(cfg, W_gate, W_up, W_down));
+    MOE_TRY(check_shared(cfg, Ws_gate, Ws_up, Ws_down));
+    MOE_TRY(need(dW_r, 16));
+    MOE_TRY(need(dW_gate, 16));
+    MOE_TRY(need(dW_up, 16));
+    MOE_TRY(need(dW_down, 16));
+    if (db) MOE_TRY(need(db, 4));
+    if (cfg->n_shared > 0) {
+        MOE_TRY(need(dWs_gate, 16));
+        MOE_TRY(need(dWs_up, 16));
+        MOE_TRY(need(dWs_down, 16));
+    }
+    if (cfg->N > 0) {
+        MOE_TRY(need(x, 16));
+        MOE_TRY(need(dout, 16));
+        MOE_TRY(need(dx, 16));
+    }
+    const WsLayout L = ws_layout(*cfg);
+    BwdArgs a{};
+    a.cfg = cfg;
+    a.x = x;
+    a.W_r = W_r;
+    a.b_r = cfg->bias_mode != 0 ? b_r : nullptr;
+    a.Wg = (const __nv_bfloat16*)W_gate;
+    a.Wu = (const __nv_bfloat16*)W_up;
+    a.Wd = (const __nv_bfloat16*)W_down;
+    a.Wsg = (const __nv_bfloat16*)Ws_gate;
+    a.Wsu = (const __nv_bfloat16*)Ws_up;
+    a.Wsd = (const __nv_bfloat16*)Ws_down;
+    a.dout = (const __nv_bfloat16*)dout;
+    a.aux_coef = aux_coef;
+    a.z_coef = z_coef;
+    a.dx = dx;
+    a.dW_r = dW_r;
+    a.db = db;
+    a.dWg = dW_gate;
+    a.dWu = dW_up;
+    a.dWd = dW_down;
+    a.dWsg = dWs_gate;
+    a.dWsu = dWs_up;
+    a.dWsd = dWs_down;
+    a.idx = at<int32_t>(ws, L.idx);
+    a.pos = at<int32_t>(ws, L.pos);
+    a.counts = at<int32_t>(ws, L.counts);
+    a.kept = at<int32_t>(ws, L.kept);
+    a.kept_off = at<int32_t>(ws, L.kept_offsets);
+    a.row_token = at<int32_t>(ws, L.row_token);
+    a.err = at<int32_t>(ws, L.err);
+    a.w = at<float>(ws, L.w);
+    a.gap = at<float>(ws, L.gap);
+    a.lse = at<float>(ws, L.lse);
+    a.p_part = at<float>(ws, L.p_part);
+    a.P_sum = at<float>(ws, L.P_sum);
+    a.row_weight = at<float>(ws, L.row_weight);
+    a.logits = at<float>(ws, L.logits);
+    a.w3 = at<__nv_bfloat16>(ws, L.router_w3);
+    a.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+    a.h_perm = at<__nv_bfloat16>(ws, L.h_perm);
+    a.h_sh = at<__nv_bfloat16>(ws, L.h_sh);
+    a.bws = bws;
+    MOE_CUDA(run_backward(a, (cudaStream_t)stream));
     return MOE_OK;
 }
 

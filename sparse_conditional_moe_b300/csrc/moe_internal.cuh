@@ -51,11 +51,12 @@ WsLayout ws_layout(const moe_cfg& c);
 // ------------------------------------------------------------------ launches
 // All return cudaGetLastError() of their launches.
 
-// lse [N] (nullable): log-sum-exp of each token's logits, for the z-loss.
+// lse [N] (nullable): log-sum-exp of each token's logits, for the z-loss; probs [N, E]
+// (nullable): the softmax probabilities, for the backward pass.
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* lse, float* p_part,
                           float* P_sum, __nv_bfloat16* w3, float* logits, int32_t* err,
-                          cudaStream_t s);
+                          cudaStream_t s, float* probs = nullptr);
 
 // Tensor-core router logits [N, E] (fp32) for bf16 x (see router_tc.cu).
 cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,

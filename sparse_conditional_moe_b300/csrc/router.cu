@@ -57,7 +57,8 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
                                              int32_t* __restrict__ idx_out,
                                              float* __restrict__ w_out,
                                              float* __restrict__ gap_out,
-                                             float* __restrict__ lse_out, float (&pacc)[NV]) {
+                                             float* __restrict__ lse_out,
+                                             float* __restrict__ probs_out, float (&pacc)[NV]) {
     const int lane = threadIdx.x & 31;
     float m = -FLT_MAX;
 #pragma unroll
@@ -85,6 +86,7 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
         const int e = lane + 32 * i;
         v[i] = (e < E) ? v[i] / s : -1.f;   // -1: never selected
         if (e < E) pacc[i] += v[i];
+        if (e < E && probs_out) probs_out[tok * E + e] = v[i];
     }
     // selection scores: the probabilities, or p + b for the selection-only bias
     float sv[NV];
@@ -186,7 +188,7 @@ router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
                    const float* __restrict__ b_r, int bias_mode, int64_t N, int d, int E, int k, int renorm,
                    int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                    float* __restrict__ gap_out, float* __restrict__ lse_out,
-                   float* __restrict__ p_part) {
+                   float* __restrict__ probs_out, float* __restrict__ p_part) {
     __shared__ float sm[kWarps * 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = (int64_t)blockIdx.x * kGemvTokensPerBlock + warp * kGemvTokensPerWarp;
@@ -244,7 +246,7 @@ router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
 #pragma unroll
         for (int e = 0; e < EP; e++)
             if (e == lane) v[0] = acc[t][e];
-        finish_token<1>(v, b_r, bias_mode, E, k, renorm, t0 + t, idx_out, w_out, gap_out, lse_out, pacc);
+        finish_token<1>(v, b_r, bias_mode, E, k, renorm, t0 + t, idx_out, w_out, gap_out, lse_out, probs_out, pacc);
     }
     write_p_part<1>(pacc, sm, E, p_part);
 }
@@ -259,7 +261,8 @@ logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b
                    int64_t N,
                    int E, int k, int renorm, int32_t* __restrict__ idx_out,
                    float* __restrict__ w_out, float* __restrict__ gap_out,
-                   float* __restrict__ lse_out, float* __restrict__ p_part) {
+                   float* __restrict__ lse_out, float* __restrict__ probs_out,
+                   float* __restrict__ p_part) {
     __shared__ float sm[kWarps * 32 * NV];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float pacc[NV];
@@ -274,7 +277,7 @@ logits_topk_kernel(const float* __restrict__ logits, const float* __restrict__ b
             const int e = lane + 32 * i;
             v[i] = e < E ? logits[tok * E + e] : 0.f;
         }
-        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, lse_out, pacc);
+        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, lse_out, probs_out, pacc);
     }
     write_p_part<NV>(pacc, sm, E, p_part);
 }
@@ -300,7 +303,7 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
                     const float* __restrict__ b_r, int bias_mode, int64_t N, int d, int E, int k, int renorm,
                     int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                     float* __restrict__ gap_out, float* __restrict__ lse_out,
-                   float* __restrict__ p_part) {
+                   float* __restrict__ probs_out, float* __restrict__ p_part) {
     using Tl = RouterTile<EP>;
     constexpr int TT = Tl::TT, TE = Tl::TE, BT = Tl::BT, DK = Tl::DK, NV = Tl::NV;
     static_assert(Tl::SMEM_FLOATS >= kWarps * EP, "P table must fit the staging buffer");
@@ -382,7 +385,7 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
         float v[NV];
 #pragma unroll
         for (int i = 0; i < NV; i++) v[i] = Ls[t * (EP + 1) + lane + 32 * i];
-        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, lse_out, pacc);
+        finish_token<NV>(v, b_r, bias_mode, E, k, renorm, tok, idx_out, w_out, gap_out, lse_out, probs_out, pacc);
     }
     __syncthreads();             // every warp is done reading the logits
     write_p_part<NV>(pacc, sm, E, p_part);
@@ -411,48 +414,48 @@ int pad_experts(int E) {
 template <typename Kernel, typename T>
 void launch_k(Kernel kern, int blocks, cudaStream_t s, const T* x, const float* W_r,
               const float* bias, const moe_cfg& c, int32_t* idx, float* w, float* gap,
-              float* lse, float* p_part) {
+              float* lse, float* probs, float* p_part) {
     kern<<<blocks, kRouterThreads, 0, s>>>(x, W_r, bias, c.bias_mode, c.N, c.d, c.E, c.k, c.renorm, idx, w,
-                                           gap, lse, p_part);
+                                           gap, lse, probs, p_part);
 }
 
 template <int EP, typename T>
 int launch_gemv(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
-                float* w, float* gap, float* lse, float* p_part, cudaStream_t s) {
+                float* w, float* gap, float* lse, float* probs, float* p_part, cudaStream_t s) {
     const int blocks = (int)((c.N + kGemvTokensPerBlock - 1) / kGemvTokensPerBlock);
-    launch_k(router_gemv_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, lse, p_part);
+    launch_k(router_gemv_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, lse, probs, p_part);
     return blocks;
 }
 
 template <int EP, typename T>
 int launch_tiled(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
-                 float* w, float* gap, float* lse, float* p_part, cudaStream_t s) {
+                 float* w, float* gap, float* lse, float* probs, float* p_part, cudaStream_t s) {
     const int blocks = (int)((c.N + RouterTile<EP>::BT - 1) / RouterTile<EP>::BT);
-    launch_k(router_tiled_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, lse, p_part);
+    launch_k(router_tiled_kernel<EP, T>, blocks, s, x, W_r, bias, c, idx, w, gap, lse, probs, p_part);
     return blocks;
 }
 
 template <int NV>
 int launch_topk(const moe_cfg& c, const float* logits, const float* bias, int32_t* idx, float* w,
-                float* gap, float* lse, float* p_part, cudaStream_t s) {
+                float* gap, float* lse, float* probs, float* p_part, cudaStream_t s) {
     const int blocks = (int)((c.N + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock);
     logits_topk_kernel<NV><<<blocks, kRouterThreads, 0, s>>>(logits, bias, c.bias_mode, c.N, c.E, c.k, c.renorm,
-                                                             idx, w, gap, lse, p_part);
+                                                             idx, w, gap, lse, probs, p_part);
     return blocks;
 }
 
 template <typename T>
 int dispatch_simt(const moe_cfg& c, const T* x, const float* W_r, const float* bias, int32_t* idx,
-                  float* w, float* gap, float* lse, float* p_part, cudaStream_t s) {
+                  float* w, float* gap, float* lse, float* probs, float* p_part, cudaStream_t s) {
     switch (pad_experts(c.E)) {
-        case 8: return launch_gemv<8>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 16: return launch_gemv<16>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 32: return launch_gemv<32>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 64: return launch_tiled<64>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 128: return launch_tiled<128>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 256: return launch_tiled<256>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        case 512: return launch_tiled<512>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
-        default: return launch_tiled<1024>(c, x, W_r, bias, idx, w, gap, lse, p_part, s);
+        case 8: return launch_gemv<8>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 16: return launch_gemv<16>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 32: return launch_gemv<32>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 64: return launch_tiled<64>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 128: return launch_tiled<128>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 256: return launch_tiled<256>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        case 512: return launch_tiled<512>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
+        default: return launch_tiled<1024>(c, x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
     }
 }
 
@@ -465,7 +468,7 @@ int64_t router_part_rows(int64_t N) { return (N + 7) / 8 + 1; }
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* lse, float* p_part,
                           float* P_sum, __nv_bfloat16* w3, float* logits, int32_t* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, float* probs) {
     const float* bias = c.bias_mode != 0 ? b_r : nullptr;
     int blocks = 0;
     if (c.N > 0) {
@@ -474,16 +477,16 @@ cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, con
                                              logits, err, s);
             if (e != cudaSuccess) return e;
             switch (pad_experts(c.E) / 32) {
-                case 1: case 2: blocks = launch_topk<2>(c, logits, bias, idx, w, gap, lse, p_part, s); break;
-                case 4: blocks = launch_topk<4>(c, logits, bias, idx, w, gap, lse, p_part, s); break;
-                case 8: blocks = launch_topk<8>(c, logits, bias, idx, w, gap, lse, p_part, s); break;
-                case 16: blocks = launch_topk<16>(c, logits, bias, idx, w, gap, lse, p_part, s); break;
-                default: blocks = launch_topk<32>(c, logits, bias, idx, w, gap, lse, p_part, s); break;
+                case 1: case 2: blocks = launch_topk<2>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;
+                case 4: blocks = launch_topk<4>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;
+                case 8: blocks = launch_topk<8>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;
+                case 16: blocks = launch_topk<16>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;
+                default: blocks = launch_topk<32>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;
             }
         } else if (c.act_dtype == MOE_BF16) {
-            blocks = dispatch_simt(c, (const __nv_bfloat16*)x, W_r, bias, idx, w, gap, lse, p_part, s);
+            blocks = dispatch_simt(c, (const __nv_bfloat16*)x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
         } else {
-            blocks = dispatch_simt(c, (const float*)x, W_r, bias, idx, w, gap, lse, p_part, s);
+            blocks = dispatch_simt(c, (const float*)x, W_r, bias, idx, w, gap, lse, probs, p_part, s);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

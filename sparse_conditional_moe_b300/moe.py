@@ -27,7 +27,7 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
            "moe_selftest_wait_timeout", "moe_status_string", "moe_quantize_w4",
            "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats",
-           "moe_selftest_gemm")
+           "moe_selftest_gemm", "moe_backward_workspace_size", "moe_backward")
 MOE_W4_GROUP = 128
 
 
@@ -103,6 +103,9 @@ def lib():
             "moe_forward_w4a16": [C, P, P, P, ctypes.POINTER(MoeW4Layer), P, P, SZ, P, P],
             "moe_router_stats": [C, P, P, P, P, P, ctypes.POINTER(MoeRouterSummary), P, SZ, P],
             "moe_selftest_gemm": [ctypes.c_int32] * 5 + [P, P, P, P, SZ, P],
+            "moe_backward_workspace_size": [C, ctypes.POINTER(SZ)],
+            "moe_backward": [C] + [P] * 10 + [ctypes.c_double, ctypes.c_double] + [P] * 9
+                            + [P, SZ, P, SZ, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -286,6 +289,29 @@ def moe_forward_w4a16(cfg, x, W_r, b_r, w4: dict, out, ws, stream=None, events=N
                                    _event_array(events, stream)), "moe_forward_w4a16")
 
 
+# ------------------------------------------------------------------ backward
+
+def moe_backward_workspace_size(cfg: MoeCfg) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_backward(cfg, x, W_r, b_r, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, dout, grads: dict,
+                 ws, bws, aux_coef: float = 0.0, z_coef: float = 0.0, stream=None):
+    """grads: dict of fp32 device tensors dx, dW_r, db (optional), dW_gate, dW_up, dW_down and,
+    with shared experts, dWs_gate, dWs_up, dWs_down (see include/moe.h)."""
+    g = grads
+    _check(lib().moe_backward(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W_gate), _p(W_up),
+                              _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down), _p(dout),
+                              float(aux_coef), float(z_coef), _p(g["dx"]), _p(g["dW_r"]),
+                              _p(g.get("db")), _p(g["dW_gate"]), _p(g["dW_up"]), _p(g["dW_down"]),
+                              _p(g.get("dWs_gate")), _p(g.get("dWs_up")), _p(g.get("dWs_down")),
+                              _p(ws), ws.numel(), _p(bws), bws.numel(), _s(stream)),
+           "moe_backward")
+
+
 def moe_forward_buffers(cfg, ws) -> dict:
     """Device tensors viewing the intermediates moe_forward leaves in the workspace."""
     b = MoeBuffers()
@@ -384,6 +410,7 @@ class MoELayer:
 
     def forward(self, x: torch.Tensor, stream=None, events=None) -> torch.Tensor:
         w = self.w
+        self.last_x = x
         if self.w4 is not None:
             moe_forward_w4a16(self.cfg, x, w["W_r"], w.get("b_r"), self.w4, self.out, self.ws,
                               stream, events)
@@ -405,6 +432,26 @@ class MoELayer:
         b = self.buffers()
         return moe_router_stats(self.cfg, b["lse"], b["w"], b["perm"], b["offsets"], self.ws,
                                 stream)
+
+    def backward(self, dout: torch.Tensor, aux_coef: float = 0.0, z_coef: float = 0.0,
+                 stream=None) -> dict:
+        """Gradients (fp32) of <dout, out> + aux_coef L_aux + z_coef L_z for the last forward."""
+        c, w = self.cfg, self.w
+        if self.w4 is not None:
+            raise MoeError(2, "backward with W4A16 weights")
+        if getattr(self, "bws", None) is None:
+            self.bws = torch.empty(moe_backward_workspace_size(c), dtype=torch.uint8,
+                                   device=self.device)
+        f = lambda *shape: torch.empty(shape, dtype=torch.float32, device=self.device)
+        E, d, F, S, Fs = c.E, c.d, c.d_ff, c.n_shared, c.d_ff_shared
+        g = dict(dx=f(c.N, d), dW_r=f(E, d), db=f(E), dW_gate=f(E, F, d), dW_up=f(E, F, d),
+                 dW_down=f(E, d, F))
+        if S > 0:
+            g.update(dWs_gate=f(S, Fs, d), dWs_up=f(S, Fs, d), dWs_down=f(S, d, Fs))
+        moe_backward(c, self.last_x, w["W_r"], w.get("b_r"), w["W_gate"], w["W_up"], w["W_down"],
+                     w.get("Ws_gate"), w.get("Ws_up"), w.get("Ws_down"), dout, g, self.ws, self.bws,
+                     aux_coef, z_coef, stream)
+        return g
 
     def device_error(self, stream=None) -> int:
         return moe_device_error(self.ws, stream)
