@@ -200,6 +200,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the batch size N (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--backward", type=int, default=10,
+                    help="timed moe_backward iterations after the forward measurement (0: none)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU-oracle budget for the cpu_baseline field (0 to skip)")
     args = ap.parse_args()
@@ -311,6 +313,34 @@ def main():
     e2e_value = spec.N * world / (e2e_ms / 1e3)
 
     # router 2, permute 4, m-tile plan 1 (not on the W4A16 path), routed 2, shared 2, combine 1
+    # ---------------- backward pass (bf16 layers whose fp32 weight gradients fit comfortably)
+    bwd = None
+    grad_bytes = 4.0 * (3 * spec.E * spec.d * spec.d_ff + 3 * spec.n_shared * spec.d * spec.d_ff_shared)
+    if (args.backward > 0 and not spec.w4a16 and spec.dtype == "bf16" and grad_bytes <= 24e9
+            and spec.d % 64 == 0 and spec.d_ff % 128 == 0):
+        dout = torch.randn(lay.out.shape, device="cuda").to(torch.bfloat16)
+        lay.forward(xs[0])
+        for _ in range(2):
+            lay.backward(dout)
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.backward):
+            lay.backward(dout)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        if lay.device_error() != 0:
+            raise RuntimeError("device error in the backward pass")
+        bwd_ms = b0.elapsed_time(b1) / args.backward
+        # expert GEMM work of the backward: 2x the forward's (data and weight gradients)
+        bwd_flops = 2.0 * (accounting.gateup_flops(spec.d, spec.d_ff, kept_rows)
+                           + accounting.down_flops(spec.d, spec.d_ff, kept_rows)
+                           + 6.0 * spec.d * spec.d_ff_shared * spec.N * spec.n_shared)
+        bwd = {"ms": bwd_ms, "tokens_per_s": spec.N * world / (bwd_ms / 1e3),
+               "expert_tflops": bwd_flops / (bwd_ms / 1e3) / 1e12, "iterations": args.backward,
+               "note": "moe_backward after one forward, all gradients fp32; the expert GEMMs do 2x "
+                       "the forward's work (gate/up recomputed once more on top)"}
+
     launches_per_step = 2 + 4 + (0 if spec.w4a16 else 1) + 2 + (2 if spec.n_shared > 0 else 0) + 1
     gemm_kernel = ("grouped W4A16 gate/up SwiGLU (CUDA cores, FFMA2)" if spec.w4a16
                    else "grouped gate/up SwiGLU GEMM (tcgen05)")
@@ -343,7 +373,7 @@ def main():
             "layer": {"tflops": layer_tflops, "hbm_gbs_alg": layer_gbs,
                       "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s * 1e3 / ms_step,
                       "kept_rows": kept_rows, "touched_experts": touched,
-                      "phase_ms": ph_ms, "phase_roofline": phase_roof},
+                      "phase_ms": ph_ms, "phase_roofline": phase_roof, "backward": bwd},
             "roofline": ({"kernel": gemm_kernel, "bound": "tensor",
                           "achieved": achieved_t, "peak": peak_t, "unit": "TFLOP/s",
                           "frac": achieved_t / peak_t, "traffic": traffic,

@@ -14,7 +14,8 @@
 //      dW_down (G4), dW_gate / dW_up (G5); the same for the shared experts;
 //   5. router backward per token: dw -> dp through the renormalisation, + aux term, softmax
 //      backward, + z term -> dl [N, E]; db = sum_t dl (bias_mode 1);
-//   6. dW_r = dl^T x and the router's part of dx = dl W_r (fp32 CUDA-core GEMMs);
+//   6. dW_r = dl^T x and the router's part of dx = dl W_r (tensor cores, fp32 operands split
+//      into bf16 pieces);
 //   7. dx per token: its kept rows of dX + the shared experts' dX + the router part (fp32).
 #include "bwd_internal.cuh"
 
@@ -140,20 +141,26 @@ router_bwd_kernel(int64_t N, int E, int k, int renorm, const float* __restrict__
         p[i] = e < E ? probs[t * E + e] : 0.f;
         dp[i] = e < E ? (float)(aux_coef * (double)E * ((double)counts[e] / A) / (double)N) : 0.f;
     }
-    // routing weights -> selected probabilities (slot order, same on every lane)
-    float ssel = 0.f, wdw = 0.f;
-    for (int j = 0; j < k; j++) {
-        const int e = idx[t * k + j];
-        const int pj = pos[t * k + j];
-        const float dwj = pj >= 0 ? dw_row[pj] : 0.f;
-        ssel += probs[t * E + e];
-        wdw += w[t * k + j] * dwj;
+    // routing weights -> selected probabilities: lane j < k loads slot j, then warp sums
+    int ej = 0;
+    float wj = 0.f, dwj = 0.f, pj = 0.f;
+    if (lane < k) {
+        ej = idx[t * k + lane];
+        const int posj = pos[t * k + lane];
+        wj = w[t * k + lane];
+        dwj = posj >= 0 ? dw_row[posj] : 0.f;
+        pj = probs[t * E + ej];
     }
+    float ssel = pj, wdw = wj * dwj;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ssel += __shfl_xor_sync(0xffffffffu, ssel, off);
+        wdw += __shfl_xor_sync(0xffffffffu, wdw, off);
+    }
+    const float addj = renorm ? (dwj - wdw) / ssel : dwj;
     for (int j = 0; j < k; j++) {
-        const int e = idx[t * k + j];
-        const int pj = pos[t * k + j];
-        const float dwj = pj >= 0 ? dw_row[pj] : 0.f;
-        const float add = renorm ? (dwj - wdw) / ssel : dwj;
+        const int e = __shfl_sync(0xffffffffu, ej, j);
+        const float add = __shfl_sync(0xffffffffu, addj, j);
 #pragma unroll
         for (int i = 0; i < NV; i++)
             if (lane + 32 * i == e) dp[i] += add;
@@ -172,60 +179,85 @@ router_bwd_kernel(int64_t N, int E, int k, int renorm, const float* __restrict__
     }
 }
 
-// db[e] = sum_t dl[t, e]: one warp per expert, lanes strided over tokens, fixed butterfly.
-__global__ void db_kernel(const float* __restrict__ dl, int64_t N, int E, float* __restrict__ db) {
-    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (e >= E) return;
-    double s = 0.0;
-    for (int64_t t = lane; t < N; t += 32) s += (double)dl[t * E + e];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) db[e] = (float)s;
+// The router GEMMs run on the tensor cores with fp32 operands split into bf16 pieces:
+// v = hi + lo + O(2^-17 |v|) with hi = bf16(v), lo = bf16(v - hi) (v - hi is exact in fp32).
+//   dx_r = dl W_r  ~ dl_hi W_hi + dl_hi W_lo + dl_lo W_hi   (K = 3E: A = [hi | hi | lo],
+//                                                              B = [W_hi; W_lo; W_hi])
+//   dW_r = dl^T x  = dl_hi^T x + dl_lo^T x                  (K = 2N: A = [hi; lo], B = [x; x])
+// (x is bf16 already).  The products are exact; the fp32 accumulation matches a plain fp32
+// GEMM to within its own rounding.
+// Row widths are padded to multiples of 8 elements (16-byte TMA strides) with zeros:
+// dl3 [N, K3], K3 = roundup(3E, 8); dlT2 [2N, Ep], Ep = roundup(E, 8); w3 [K3, d].
+__host__ __device__ inline int pad8(int v) { return (v + 7) / 8 * 8; }
+
+__global__ void split_dl_kernel(const float* __restrict__ dl, int64_t N, int E,
+                                __nv_bfloat16* __restrict__ dl3, __nv_bfloat16* __restrict__ dlT2) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N * E) return;
+    const int64_t t = i / E;
+    const int e = (int)(i - t * E);
+    const int K3 = pad8(3 * E), Ep = pad8(E);
+    const float v = dl[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    dl3[t * K3 + e] = hi;
+    dl3[t * K3 + E + e] = hi;
+    dl3[t * K3 + 2 * E + e] = lo;
+    dlT2[t * Ep + e] = hi;
+    dlT2[(N + t) * Ep + e] = lo;
 }
 
-// C[M, N] = sum_k A(m, k) B(k, n) in fp32 on CUDA cores, 64x64 tiles, 16-deep k slices.
-// A(m, k) = A[m * sam + k * sak]; B(k, n) = B[k * sbk + n * sbn] (fp32 or bf16 B).
-template <typename TB>
-__global__ void __launch_bounds__(256)
-f32_gemm_kernel(int M, int N, int64_t K, const float* __restrict__ A, int64_t sam, int64_t sak,
-                const TB* __restrict__ B, int64_t sbk, int64_t sbn, float* __restrict__ C,
-                int64_t ldc) {
-    __shared__ float As[16][64 + 1];
-    __shared__ float Bs[16][64 + 1];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-    float acc[4][4] = {};
-    for (int64_t k0 = 0; k0 < K; k0 += 16) {
-        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int kk = i / 64, mm = i % 64;
-            const int64_t k = k0 + kk;
-            As[kk][mm] = (m0 + mm < M && k < K) ? A[(int64_t)(m0 + mm) * sam + k * sak] : 0.f;
-            Bs[kk][mm] = (n0 + mm < N && k < K) ? (float)B[k * sbk + (int64_t)(n0 + mm) * sbn] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < 16; kk++) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                a[i] = As[kk][ty * 4 + i];
-                b[i] = Bs[kk][tx * 4 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-#pragma unroll
-                for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
+__global__ void split_wr_kernel(const float* __restrict__ W, int E, int d,
+                                __nv_bfloat16* __restrict__ w3) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)E * d) return;
+    const float v = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    w3[i] = hi;
+    w3[(int64_t)E * d + i] = lo;
+    w3[2 * (int64_t)E * d + i] = hi;
+}
+
+// x2 = [x; x] (2N rows)
+__global__ void dup_rows_kernel(const uint4* __restrict__ x, int64_t n16, uint4* __restrict__ x2) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n16) return;
+    const uint4 v = x[i];
+    x2[i] = v;
+    x2[n16 + i] = v;
+}
+
+// One group of `rows` rows at offset 0 (a_off = c_off = {0, pad}, dense_off = {0}).
+__global__ void plan_single_kernel(int64_t rows, int64_t pad, int32_t* plan) {
+    if (threadIdx.x == 0) {
+        plan[0] = (int32_t)rows;
+        plan[1] = 0;
+        plan[2] = (int32_t)pad;
+        plan[3] = 0;
     }
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
-            if (m < M && n < N) C[(int64_t)m * ldc + n] = acc[i][j];
-        }
+}
+
+// db partials: block b sums its token chunk for every expert (threads over experts: coalesced),
+// then db[e] = the partials in block order.
+constexpr int kDbChunks = 64;
+__global__ void db_part_kernel(const float* __restrict__ dl, int64_t N, int E,
+                               double* __restrict__ part) {
+    const int64_t per = (N + kDbChunks - 1) / kDbChunks;
+    const int64_t t0 = (int64_t)blockIdx.x * per, t1 = t0 + per < N ? t0 + per : N;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        double s = 0.0;
+        for (int64_t t = t0; t < t1; t++) s += (double)dl[t * E + e];
+        part[(int64_t)blockIdx.x * E + e] = s;
+    }
+}
+
+__global__ void db_final_kernel(const double* __restrict__ part, int E, float* __restrict__ db) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    double s = 0.0;
+    for (int b = 0; b < kDbChunks; b++) s += part[(int64_t)b * E + e];
+    db[e] = (float)s;
 }
 
 // dx[t] = sum over t's kept slots of dX[padded row] + sum_s dX_s[s * Np + t] + dx_r[t].
@@ -300,6 +332,12 @@ BwdLayout bwd_layout(const moe_cfg& c) {
     L.hw_s = take(2 * (size_t)(S * Np * Fs));
     L.dX_s = take(4 * (size_t)(S * Np * d));
     L.dw_part_s = take(4 * (size_t)(S * Np * (Fs > 0 ? Fs / 128 : 1)));
+    L.r_plan = take(4 * 8);
+    L.dl3 = take(2 * (size_t)(N * pad8(3 * (int)E)));
+    L.dlT2 = take(2 * (size_t)(2 * N * pad8((int)E)));
+    L.w3 = take(2 * (size_t)(pad8(3 * (int)E) * d));
+    L.x2 = take(2 * (size_t)(2 * N * d));
+    L.db_part = take(8 * (size_t)(kDbChunks * E));
     L.total = off;
     return L;
 }
@@ -411,7 +449,7 @@ cudaError_t run_backward(const BwdArgs& a, cudaStream_t s) {
             return e;
         dw_rows_kernel<<<(unsigned)((R + 255) / 256), 256, 0, s>>>(a.kept_off, c_off, E, R,
                                                                    at<float>(bw, L.dw_part),
-                                                                   (int)(F / 128), dw_row);
+                                                                   tb_dh_tiles((int)F), dw_row);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else {
         cudaMemsetAsync(a.dWg, 0, sizeof(float) * (size_t)(E * F * d), s);
@@ -448,21 +486,61 @@ cudaError_t run_backward(const BwdArgs& a, cudaStream_t s) {
         }
     }
     if (a.db) {
-        if (c.bias_mode == 1 && N > 0) db_kernel<<<(E + 7) / 8, 256, 0, s>>>(dl, N, E, a.db);
-        else cudaMemsetAsync(a.db, 0, sizeof(float) * (size_t)E, s);
+        if (c.bias_mode == 1 && N > 0) {
+            db_part_kernel<<<kDbChunks, 256, 0, s>>>(dl, N, E, at<double>(bw, L.db_part));
+            db_final_kernel<<<(E + 255) / 256, 256, 0, s>>>(at<double>(bw, L.db_part), E, a.db);
+        } else {
+            cudaMemsetAsync(a.db, 0, sizeof(float) * (size_t)E, s);
+        }
     }
-    // 6. router GEMMs: dW_r [E, d] = dl^T x; dx_r [N, d] = dl W_r
+    // 6. router GEMMs on the tensor cores (bf16 pieces of the fp32 operands)
     float* dx_r = at<float>(bw, L.dx_r);
-    dim3 gw((unsigned)((d + 63) / 64), (unsigned)((E + 63) / 64));
-    f32_gemm_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(E, (int)d, N, dl, 1, E,
-                                                      (const __nv_bfloat16*)a.x, d, 1, a.dW_r, d);
     if (N > 0) {
-        dim3 gx((unsigned)((d + 63) / 64), (unsigned)((N + 63) / 64));
-        f32_gemm_kernel<float><<<gx, 256, 0, s>>>((int)N, (int)d, E, dl, E, 1, a.W_r, d, 1, dx_r, d);
+        __nv_bfloat16* dl3 = at<__nv_bfloat16>(bw, L.dl3);
+        __nv_bfloat16* dlT2 = at<__nv_bfloat16>(bw, L.dlT2);
+        __nv_bfloat16* w3 = at<__nv_bfloat16>(bw, L.w3);
+        __nv_bfloat16* x2 = at<__nv_bfloat16>(bw, L.x2);
+        int32_t* rp = at<int32_t>(bw, L.r_plan);   // [0..3] dx_r group, [4..7] dW_r group
+        const int K3 = pad8(3 * E), Ep = pad8(E);
+        if (K3 != 3 * E) cudaMemsetAsync(dl3, 0, 2 * (size_t)(N * K3), s);
+        if (Ep != E) cudaMemsetAsync(dlT2, 0, 2 * (size_t)(2 * N * Ep), s);
+        if (K3 != 3 * E) cudaMemsetAsync(w3 + (size_t)3 * E * d, 0, 2 * (size_t)(K3 - 3 * E) * d, s);
+        split_dl_kernel<<<(unsigned)((N * E + 255) / 256), 256, 0, s>>>(dl, N, E, dl3, dlT2);
+        split_wr_kernel<<<(unsigned)(((int64_t)E * d + 255) / 256), 256, 0, s>>>(a.W_r, E, (int)d, w3);
+        const int64_t n16 = N * d / 8;
+        dup_rows_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, s>>>(
+            reinterpret_cast<const uint4*>(a.x), n16, reinterpret_cast<uint4*>(x2));
+        const int64_t Npad = (N + 127) / 128 * 128;
+        plan_single_kernel<<<1, 32, 0, s>>>(N, Npad, rp);
+        plan_single_kernel<<<1, 32, 0, s>>>(2 * N, 2 * N, rp + 4);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        TbParams p{};
+        p.G = 1;
+        p.rows = rp;
+        p.a_off = rp + 1;
+        p.c_off = rp + 1;
+        p.dense_off = rp + 3;
+        p.max_mtiles = Npad / 128;
+        p.err = a.err;
+        p.out_f32 = dx_r;
+        if ((e = tb_rows_f32(p, dl3, N, K3, w3, (int)d, s)) != cudaSuccess) return e;
+        TbParams q{};
+        q.G = 1;
+        q.rows = rp + 4;
+        q.a_off = rp + 5;
+        q.c_off = rp + 5;
+        q.dense_off = rp + 7;
+        q.split_m = E;
+        q.out_f32 = a.dW_r;
+        q.out_f32b = a.dW_r;
+        q.err = a.err;
+        if ((e = tb_wgrad(q, dlT2, 2 * N, E, x2, 2 * N, (int)d, s, Ep)) != cudaSuccess) return e;
         // 7. dx
         dx_combine_kernel<<<(unsigned)((N * 32 + 255) / 256), 256, 0, s>>>(
             N, k, (int)d, (int)S, Np, a.idx, a.pos, a.kept_off, c_off, at<float>(bw, L.dX),
             at<float>(bw, L.dX_s), dx_r, a.dx);
+    } else {
+        cudaMemsetAsync(a.dW_r, 0, sizeof(float) * (size_t)(E * d), s);
     }
     return cudaGetLastError();
 }

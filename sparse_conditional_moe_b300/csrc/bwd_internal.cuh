@@ -36,14 +36,18 @@ struct TbParams {
     int32_t* err;
 };
 
+int tb_dh_tiles(int F);   // column tiles of G1 (dw partials per row)
 cudaError_t tb_dh(const TbParams& p, const __nv_bfloat16* dout_pad, int64_t rows_a, int d,
                   const __nv_bfloat16* Wd, int F, cudaStream_t s);
 cudaError_t tb_swiglu_bwd(const TbParams& p, const __nv_bfloat16* x_pad, int64_t rows_a, int d,
                           const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F, cudaStream_t s);
 cudaError_t tb_dx(const TbParams& p, const __nv_bfloat16* dgu, int64_t rows_a, int F,
                   const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int d, cudaStream_t s);
+cudaError_t tb_rows_f32(const TbParams& p, const __nv_bfloat16* A, int64_t rows_a, int K,
+                        const __nv_bfloat16* B, int N, cudaStream_t s);
 cudaError_t tb_wgrad(const TbParams& p, const __nv_bfloat16* A, int64_t rows_a, int M,
-                     const __nv_bfloat16* B, int64_t rows_b, int N, cudaStream_t s);
+                     const __nv_bfloat16* B, int64_t rows_b, int N, cudaStream_t s,
+                     int a_cols = 0);
 cudaError_t tb_selftest(bool a_mn, bool b_mn, int M, int N, int K, const __nv_bfloat16* A,
                         const __nv_bfloat16* B, float* C, const int32_t* plan, int32_t* err,
                         cudaStream_t s);
@@ -52,6 +56,7 @@ cudaError_t tb_selftest(bool a_mn, bool b_mn, int M, int N, int K, const __nv_bf
 
 struct BwdLayout {   // byte offsets in the backward workspace (256-byte aligned regions)
     size_t probs, dl, dx_r, dw_row, c_off, s_plan;
+    size_t r_plan, dl3, dlT2, w3, x2, db_part;   // router GEMMs on the tensor cores
     size_t dout_pad, x_pad, dh, dgu, hw, dX, dw_part;
     size_t dout_s, x_s, dh_s, dgu_s, hw_s, dX_s, dw_part_s;
     size_t total;

@@ -13,12 +13,13 @@
 // The same kernels serve the shared experts (one group of N rows each, weight 1).
 //
 // Design (one CTA per SM, persistent, warp-specialised, 192 threads), as the forward kernel:
-//   warp 0      TMA producer: A tile 128x64 and B tile 128x64 (bf16, 128-byte swizzle) per
-//               k-block into a 4-stage ring.  A K-major operand is one box of 128 rows x 64;
-//               an MN-major operand is two boxes of 64 k-rows x 64 elements (8 KB apart);
-//   warp 1      allocates 256 TMEM columns; one thread issues tcgen05.mma (M=128, N=128,
+//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128-byte swizzle) per
+//               k-block into a 4-stage ring (48 KB per stage).  A K-major operand is one box
+//               of its rows x 64; an MN-major operand is boxes of 64 k-rows x 64 elements,
+//               8 KB apart (two for A, four for B);
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
 //               K=16) with the operands' majorness in the instruction descriptor;
-//   warps 2..5  epilogue: tcgen05.ld of the 128x128 fp32 accumulator, per-row arithmetic,
+//   warps 2..5  epilogue: tcgen05.ld of the 128x256 fp32 accumulator, per-row arithmetic,
 //               16-byte stores.  Two accumulators overlap epilogue and mainloop.
 // Every wait is bounded (globaltimer); on expiry the CTA raises an abort flag, drains, frees
 // TMEM and sets MOE_DEVERR_TIMEOUT.
@@ -30,9 +31,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
-constexpr int B_STAGE = BN * BK * 2;   // 16 KB
+constexpr int B_STAGE = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int MN_BOX = 64 * BK * 2;    // one MN-major box: 64 k-rows x 64 elements, 8 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -174,13 +175,14 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         const int y = t.g * p.b_rows + t.nt * (BN / 2);
                         tma_load_2d(b_dst, &tmB0, &full[s], kx, y);
                         tma_load_2d(b_dst + B_STAGE / 2, &tmB1, &full[s], kx, y);
-                    } else if (B_MN) {                     // [K rows, N]: two 64-wide boxes
+                    } else if (B_MN) {                     // [K rows, N]: four 64-wide boxes
                         const bool second = rows_mode && kx >= p.k_split;
                         const CUtensorMap* m = second ? &tmB1 : &tmB0;
                         const int b_k = rows_mode ? t.g * p.b_rows + (second ? kx - p.k_split : kx)
                                                   : p.c_off[t.g] + kx;
-                        tma_load_2d(b_dst, m, &full[s], t.nt * BN, b_k);
-                        tma_load_2d(b_dst + MN_BOX, m, &full[s], t.nt * BN + 64, b_k);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++)
+                            tma_load_2d(b_dst + j * MN_BOX, m, &full[s], t.nt * BN + 64 * j, b_k);
                     } else {                               // [N rows, K]: one box of BN rows
                         const int b_k = (rows_mode ? 0 : p.c_off[t.g]) + kx;
                         const int b_n = (rows_mode ? t.g * p.b_rows : 0) + t.nt * BN;
@@ -300,6 +302,7 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         tmem_ld32(taddr + c * 32, a);
                         tmem_ld_wait();
                         const int col = t.nt * BN + c * 32;
+                        if (col >= p.N) continue;         // ragged last tile (F % 256 != 0)
                         uint32_t pk[16];
                         if (valid) {
                             const uint4* hp = reinterpret_cast<const uint4*>(p.aux_bf16 + dr * p.ld_aux + col);
@@ -442,6 +445,8 @@ bool map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
 
 }  // namespace
 
+int tb_dh_tiles(int F) { return (F + BN - 1) / BN; }
+
 // G1: dh = w * (dout_pad . W_d), dw partials.  dout_pad [rows_a, d] (a_off rows), W_d [G*d, F].
 cudaError_t tb_dh(const TbParams& p0, const __nv_bfloat16* dout_pad, int64_t rows_a, int d,
                   const __nv_bfloat16* Wd, int F, cudaStream_t s) {
@@ -454,7 +459,7 @@ cudaError_t tb_dh(const TbParams& p0, const __nv_bfloat16* dout_pad, int64_t row
     p.k_split = d;
     p.b_rows = d;
     p.N = F;
-    p.n_tiles = F / BN;
+    p.n_tiles = tb_dh_tiles(F);
     return launch_tb<false, true, TBE_DH>(ma, mb, mb, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
@@ -492,12 +497,30 @@ cudaError_t tb_dx(const TbParams& p0, const __nv_bfloat16* dgu, int64_t rows_a, 
     return launch_tb<false, true, TBE_ROWS_F32>(ma, mg, mu, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
+// Rows GEMM of one operand pair: out[r, :] (fp32) = A[a_off + r, :K] (K-major) . B[k, :N]
+// (B [K rows, N], MN-major), for the group rows given in p (the router's part of dx).
+cudaError_t tb_rows_f32(const TbParams& p0, const __nv_bfloat16* A, int64_t rows_a, int K,
+                        const __nv_bfloat16* B, int N, cudaStream_t s) {
+    CUtensorMap ma, mb;
+    if (!map_bf16(&ma, A, rows_a, K, 64, BM) || !map_bf16(&mb, B, K, N, 64, 64))
+        return cudaErrorInvalidValue;
+    TbParams p = p0;
+    p.mode = TB_ROWS;
+    p.K = K;
+    p.k_split = K;
+    p.b_rows = 0;
+    p.N = N;
+    p.n_tiles = (N + BN - 1) / BN;
+    return launch_tb<false, true, TBE_ROWS_F32>(ma, mb, mb, p, p.max_mtiles * (int64_t)p.n_tiles, s);
+}
+
 // Weight gradients: out[g] (M x N fp32, rows < split_m into out_f32, the rest into out_f32b)
 // = sum over the group's padded rows r of A[a_off + r, m] * B[c_off + r, n].
+// (a_cols >= M: A's row width in memory when its rows are padded; 0 = M.)
 cudaError_t tb_wgrad(const TbParams& p0, const __nv_bfloat16* A, int64_t rows_a, int M,
-                     const __nv_bfloat16* B, int64_t rows_b, int N, cudaStream_t s) {
+                     const __nv_bfloat16* B, int64_t rows_b, int N, cudaStream_t s, int a_cols) {
     CUtensorMap ma, mb;
-    if (!map_bf16(&ma, A, rows_a, M, 64, 64) || !map_bf16(&mb, B, rows_b, N, 64, 64))
+    if (!map_bf16(&ma, A, rows_a, a_cols > 0 ? a_cols : M, 64, 64) || !map_bf16(&mb, B, rows_b, N, 64, 64))
         return cudaErrorInvalidValue;
     TbParams p = p0;
     p.mode = TB_WEIGHTS;

@@ -93,3 +93,34 @@ def test_backward_rejects_unsupported_layers():
     cfg = moe.cfg_from_spec(spec)
     with pytest.raises(moe.MoeError):
         moe.moe_backward_workspace_size(cfg)
+
+
+def test_backward_full_size_mixtral_sampled_tokens():
+    """At the Mixtral-shaped size (no capacity, aux and z off) a token's dx depends on that token
+    alone, so the oracle's backward of a sampled sub-batch gives its exact reference."""
+    spec = moe_synth.MIXTRAL
+    torch.cuda.empty_cache()
+    dev = moe_synth.make_layer(spec, seed=0, device="cuda")
+    lay = moe.MoELayer(moe.cfg_from_spec(spec), dev)
+    lay.forward(dev["x"])
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    dout = torch.randn((spec.N, spec.d), generator=gen, device="cuda").to(torch.bfloat16)
+    g = lay.backward(dout)
+    torch.cuda.synchronize()
+    assert lay.device_error() == 0
+    for name in ("dW_gate", "dW_up", "dW_down", "dW_r"):
+        assert torch.isfinite(g[name]).all()
+    assert all(g["dW_down"][e].abs().max() > 0 for e in range(spec.E))
+    tok = moe_synth.sample_tokens(spec.N, 6, seed=2).numpy()
+    host = {n: (None if dev[n] is None else dev[n].cpu()) for n in dev}
+    sub = dict(host)
+    sub["x"] = host["x"][tok]
+    idx_o, _, _, gap_o = oracle.route(sub["x"], host["W_r"], None, spec.k, oracle.BF16)
+    assert np.all(gap_o > 1e-6)
+    assert np.array_equal(lay.buffers()["idx"].cpu().numpy()[tok], idx_o)
+    ref = oracle.backward(sub, spec.k, oracle.BF16, dout.cpu()[tok].double().numpy())
+    got = g["dx"].cpu().numpy()[tok]
+    for i in range(len(tok)):
+        assert rel(got[i], ref["dx"][i]) <= REL, (int(tok[i]), rel(got[i], ref["dx"][i]))
+    del dev, lay, g
+    torch.cuda.empty_cache()
