@@ -200,6 +200,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the batch size N (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count E (smaller cases for profiling; not a bench line)")
     ap.add_argument("--backward", type=int, default=10,
                     help="timed moe_backward iterations after the forward measurement (0: none)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -212,6 +214,9 @@ def main():
     spec = moe_synth.WORKLOADS[args.workload]
     if args.tokens > 0:
         spec = spec.with_(N=args.tokens, name=f"{spec.name}_N{args.tokens}")
+    if args.experts > 0:
+        spec = spec.with_(E=args.experts, k=min(spec.k, args.experts),
+                          name=f"{spec.name}_E{args.experts}")
     peaks, peak_src = load_peaks()
 
     if args.impl == "reference":
@@ -227,6 +232,16 @@ def main():
     dev = moe_synth.make_layer(spec, seed=0, device="cuda")
     cfg = moe.cfg_from_spec(spec)
     w4 = moe.quantize_layer_w4(dev) if spec.w4a16 else None
+    host_copy = None
+    if w4 is not None:
+        # the forward reads the 4-bit copies only: keep host bf16 weights for the oracle leg
+        # (if it runs) and free the device ones
+        if args.cpu_seconds > 0 and rank == 0:
+            host_copy = host_layer(dev)
+        for n in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
+            if dev.get(n) is not None:
+                dev[n] = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+        torch.cuda.empty_cache()
     lay = moe.MoELayer(cfg, dev, w4=w4)
     xs = [dev["x"], moe_synth.make_x(spec, seed=1000 + rank, device="cuda")]
     stream = torch.cuda.current_stream()
@@ -348,7 +363,8 @@ def main():
     # ---------------- CPU oracle on a bounded sub-batch (rank 0 only)
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
-        rate, done, secs, sub, cores = cpu_oracle_rate(spec, host_layer(dev), args.cpu_seconds)
+        rate, done, secs, sub, cores = cpu_oracle_rate(spec, host_copy or host_layer(dev),
+                                                       args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{done} tokens of {spec.name} in consecutive sub-batches of {sub} "
                          f"(each its own batch), {secs:.1f} s of CPU work"

@@ -129,17 +129,18 @@ router_bwd_kernel(int64_t N, int E, int k, int renorm, const float* __restrict__
                   const int32_t* __restrict__ idx, const float* __restrict__ w,
                   const int32_t* __restrict__ pos, const float* __restrict__ dw_row,
                   const int32_t* __restrict__ counts, const float* __restrict__ lse,
-                  double aux_coef, double z_coef, float* __restrict__ dl) {
+                  float aux_scale, float z_scale, float* __restrict__ dl) {
+    // aux_scale = aux_coef E / (N k N): dL_aux/dp_e = aux_scale * counts_e;
+    // z_scale = 2 z_coef / N: dL_z/dl_e = z_scale * lse_t * p_e
     const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= N) return;
-    const double A = (double)N * (double)k;
     float p[NV], dp[NV];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int e = lane + 32 * i;
         p[i] = e < E ? probs[t * E + e] : 0.f;
-        dp[i] = e < E ? (float)(aux_coef * (double)E * ((double)counts[e] / A) / (double)N) : 0.f;
+        dp[i] = e < E ? aux_scale * (float)counts[e] : 0.f;
     }
     // routing weights -> selected probabilities: lane j < k loads slot j, then warp sums
     int ej = 0;
@@ -171,7 +172,7 @@ router_bwd_kernel(int64_t N, int E, int k, int renorm, const float* __restrict__
     for (int i = 0; i < NV; i++) pdp += p[i] * dp[i];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) pdp += __shfl_xor_sync(0xffffffffu, pdp, off);
-    const float zt = (float)(2.0 * z_coef / (double)N) * lse[t];
+    const float zt = z_scale * lse[t];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int e = lane + 32 * i;
@@ -474,15 +475,18 @@ cudaError_t run_backward(const BwdArgs& a, cudaStream_t s) {
     }
     // 5. router backward
     float* dl = at<float>(bw, L.dl);
+    const float aux_scale =
+        N > 0 ? (float)(a.aux_coef * (double)E / ((double)N * (double)k * (double)N)) : 0.f;
+    const float z_scale = N > 0 ? (float)(2.0 * a.z_coef / (double)N) : 0.f;
     if (N > 0) {
         const unsigned blocks = (unsigned)((N * 32 + 255) / 256);
         switch (router_nv(E)) {
-            case 1: router_bwd_kernel<1><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
-            case 2: router_bwd_kernel<2><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
-            case 4: router_bwd_kernel<4><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
-            case 8: router_bwd_kernel<8><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
-            case 16: router_bwd_kernel<16><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
-            default: router_bwd_kernel<32><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, a.aux_coef, a.z_coef, dl); break;
+            case 1: router_bwd_kernel<1><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
+            case 2: router_bwd_kernel<2><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
+            case 4: router_bwd_kernel<4><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
+            case 8: router_bwd_kernel<8><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
+            case 16: router_bwd_kernel<16><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
+            default: router_bwd_kernel<32><<<blocks, 256, 0, s>>>(N, E, k, c.renorm, probs, a.idx, a.w, a.pos, dw_row, a.counts, a.lse, aux_scale, z_scale, dl); break;
         }
     }
     if (a.db) {

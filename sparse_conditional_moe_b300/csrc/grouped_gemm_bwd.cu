@@ -38,7 +38,9 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int MN_BOX = 64 * BK * 2;    // one MN-major box: 64 k-rows x 64 elements, 8 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+constexpr int STAGE_WORDS = 32 * 33;   // per epilogue warp: 32 rows x 32 words, padded
+constexpr int STAGING_BYTES = 4 * STAGE_WORDS * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
 // MN-major operand, 128-byte swizzle: 64 elements (128 B) along M or N per row, one row per k,
 // 8-row groups 1024 bytes apart (stride byte offset), the second 64-element column 8 KB away
@@ -97,6 +99,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// The warp's 32 rows x 32 words (lane = row, v = that row's words) written row by row with
+// coalesced stores, staged through the warp's padded buffer: each store instruction writes one
+// whole 128-byte row segment.  row_dst: this lane's destination for these 32 words (nullptr:
+// the row is not written); nwords: words of the segment to keep (a ragged right edge).
+__device__ __forceinline__ void store_rows32(uint32_t* buf, const uint32_t (&v)[32],
+                                             uint32_t* row_dst, int nwords) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; j++) buf[lane * 33 + j] = v[j];
+    __syncwarp();
+    const uint64_t mine = reinterpret_cast<uint64_t>(row_dst);
+#pragma unroll 4
+    for (int r = 0; r < 32; r++) {
+        const uint64_t pr = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(mine >> 32), r) << 32) |
+                            __shfl_sync(0xffffffffu, (uint32_t)mine, r);
+        if (pr != 0 && lane < nwords) reinterpret_cast<uint32_t*>(pr)[lane] = buf[r * 33 + lane];
+    }
+}
+
+// The same for 32 rows x 16 words (32 bf16 per row, 64 bytes): two rows per store instruction.
+__device__ __forceinline__ void store_rows16(uint32_t* buf, const uint32_t (&v)[16],
+                                             uint32_t* row_dst) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 16; j++) buf[lane * 17 + j] = v[j];
+    __syncwarp();
+    const uint64_t mine = reinterpret_cast<uint64_t>(row_dst);
+    const int half = lane >> 4, wdx = lane & 15;
+#pragma unroll 4
+    for (int r2 = 0; r2 < 16; r2++) {
+        const int r = 2 * r2 + half;
+        const uint64_t pr = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(mine >> 32), r) << 32) |
+                            __shfl_sync(0xffffffffu, (uint32_t)mine, r);
+        if (pr != 0) reinterpret_cast<uint32_t*>(pr)[wdx] = buf[r * 17 + wdx];
+    }
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -106,7 +147,8 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint32_t* staging = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -259,6 +301,7 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             tc_fence_after();
             const Tile t = decode(p, tile);
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            uint32_t* buf = staging + (warp - 2) * STAGE_WORDS;
             if (EPI == TBE_F32) {
                 // weight gradient rows m of group g (every lane reads TMEM: the load is
                 // warp-collective); a group without rows has no MMAs: its tile is zero
@@ -279,14 +322,9 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         for (int j = 0; j < 32; j++) a[j] = 0u;
                     }
                     const int col = t.nt * BN + c * 32;
-                    if (dst) {
-#pragma unroll
-                        for (int v = 0; v < 8; v++)
-                            if (col + v * 4 + 4 <= p.N)
-                                *reinterpret_cast<float4*>(dst + col + v * 4) =
-                                    make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
-                                                __uint_as_float(a[4 * v + 2]), __uint_as_float(a[4 * v + 3]));
-                    }
+                    if (col >= p.N) continue;              // warp-uniform
+                    store_rows32(buf, a, dst ? reinterpret_cast<uint32_t*>(dst + col) : nullptr,
+                                 min(32, p.N - col));
                 }
             } else {
                 const int rl = t.mt * BM + row_in_tile;          // row within the group
@@ -323,10 +361,7 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 #pragma unroll
                             for (int j = 0; j < 16; j++) pk[j] = 0u;
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + pr * p.ld_bf16 + col);
-#pragma unroll
-                        for (int v = 0; v < 4; v++)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        store_rows16(buf, pk, reinterpret_cast<uint32_t*>(p.out_bf16 + pr * p.ld_bf16 + col));
                     }
                     p.dw_part[pr * p.n_tiles + t.nt] = valid ? part : 0.f;
                 } else if (EPI == TBE_SWIGLU_BWD) {
@@ -368,15 +403,9 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 #pragma unroll
                             for (int j = 0; j < 16; j++) pg[j] = pu[j] = ph[j] = 0u;
                         }
-                        uint4* dg = reinterpret_cast<uint4*>(p.out_bf16 + pr * p.ld_bf16 + f);
-                        uint4* du = reinterpret_cast<uint4*>(p.out_bf16 + pr * p.ld_bf16 + p.F + f);
-                        uint4* dhw = reinterpret_cast<uint4*>(p.out2_bf16 + pr * p.F + f);
-#pragma unroll
-                        for (int v = 0; v < 4; v++) {
-                            dg[v] = make_uint4(pg[4 * v], pg[4 * v + 1], pg[4 * v + 2], pg[4 * v + 3]);
-                            du[v] = make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2], pu[4 * v + 3]);
-                            dhw[v] = make_uint4(ph[4 * v], ph[4 * v + 1], ph[4 * v + 2], ph[4 * v + 3]);
-                        }
+                        store_rows16(buf, pg, reinterpret_cast<uint32_t*>(p.out_bf16 + pr * p.ld_bf16 + f));
+                        store_rows16(buf, pu, reinterpret_cast<uint32_t*>(p.out_bf16 + pr * p.ld_bf16 + p.F + f));
+                        store_rows16(buf, ph, reinterpret_cast<uint32_t*>(p.out2_bf16 + pr * p.F + f));
                     }
                 } else {   // TBE_ROWS_F32: dX rows, fp32
 #pragma unroll 1
@@ -385,15 +414,9 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         tmem_ld32(taddr + c * 32, a);
                         tmem_ld_wait();
                         const int col = t.nt * BN + c * 32;
-                        if (valid) {
-                            float* dst = p.out_f32 + pr * p.N + col;
-#pragma unroll
-                            for (int v = 0; v < 8; v++)
-                                if (col + v * 4 + 4 <= p.N)
-                                    *reinterpret_cast<float4*>(dst + v * 4) =
-                                        make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
-                                                    __uint_as_float(a[4 * v + 2]), __uint_as_float(a[4 * v + 3]));
-                        }
+                        if (col >= p.N) continue;         // warp-uniform
+                        store_rows32(buf, a, valid ? reinterpret_cast<uint32_t*>(p.out_f32 + pr * p.N + col) : nullptr,
+                                     min(32, p.N - col));
                     }
                 }
             }
