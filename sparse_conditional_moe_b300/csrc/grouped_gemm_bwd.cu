@@ -38,8 +38,8 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int MN_BOX = 64 * BK * 2;    // one MN-major box: 64 k-rows x 64 elements, 8 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr int STAGE_WORDS = 32 * 33;   // per epilogue warp: 32 rows x 32 words, padded
-constexpr int STAGING_BYTES = 4 * STAGE_WORDS * 4;
+constexpr int STAGE_BUF = 4096;         // per epilogue warp: 2 buffers of 32 rows x 128 B
+constexpr int STAGING_BYTES = 4 * 2 * STAGE_BUF;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
 // MN-major operand, 128-byte swizzle: 64 elements (128 B) along M or N per row, one row per k,
@@ -99,23 +99,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// The warp's 32 rows x 32 words (lane = row, v = that row's words) written row by row with
-// coalesced stores, staged through the warp's padded buffer: each store instruction writes one
-// whole 128-byte row segment.  row_dst: this lane's destination for these 32 words (nullptr:
-// the row is not written); nwords: words of the segment to keep (a ragged right edge).
-__device__ __forceinline__ void store_rows32(uint32_t* buf, const uint32_t (&v)[32],
-                                             uint32_t* row_dst, int nwords) {
+// The warp's 32 rows x 32 fp32 (lane = row) to global memory through the warp's staging buffer
+// (128-byte rows, 128-byte swizzle: conflict-free 16-byte stores) and one TMA store at (col,
+// row0) of the output map; the map clips rows and columns outside the tensor.  The warp
+// alternates between two buffers: the store that used a buffer two chunks ago must have finished
+// reading it.
+__device__ __forceinline__ void store_chunk_f32(const CUtensorMap* map, uint32_t buf,
+                                                const uint32_t (&v)[32], int32_t col, int32_t row0) {
     const int lane = threadIdx.x & 31;
+    if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
+    const uint32_t rowb = buf + (uint32_t)lane * 128u;
+    const uint32_t sw = (uint32_t)lane & 7u;
 #pragma unroll
-    for (int j = 0; j < 32; j++) buf[lane * 33 + j] = v[j];
+    for (int c = 0; c < 8; c++)
+        st_shared_v4(rowb + (((uint32_t)c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                     v[4 * c + 3]);
+    fence_proxy_async_smem();
     __syncwarp();
-    const uint64_t mine = reinterpret_cast<uint64_t>(row_dst);
-#pragma unroll 4
-    for (int r = 0; r < 32; r++) {
-        const uint64_t pr = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(mine >> 32), r) << 32) |
-                            __shfl_sync(0xffffffffu, (uint32_t)mine, r);
-        if (pr != 0 && lane < nwords) reinterpret_cast<uint32_t*>(pr)[lane] = buf[r * 33 + lane];
+    if (lane == 0) {
+        tma_store_2d(map, buf, col, row0);
+        bulk_commit();
     }
 }
 
@@ -141,7 +145,8 @@ __device__ __forceinline__ void store_rows16(uint32_t* buf, const uint32_t (&v)[
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-           const __grid_constant__ CUtensorMap tmB1, const TbParams p) {
+           const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
+           const __grid_constant__ CUtensorMap tmC1, const TbParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -294,6 +299,7 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
         int it = 0;
+        int nchunk = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -301,30 +307,33 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             tc_fence_after();
             const Tile t = decode(p, tile);
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            uint32_t* buf = staging + (warp - 2) * STAGE_WORDS;
+            uint32_t* buf = staging + (warp - 2) * (2 * STAGE_BUF / 4);
+            const uint32_t sbuf = smem_u32(buf);
             if (EPI == TBE_F32) {
                 // weight gradient rows m of group g (every lane reads TMEM: the load is
                 // warp-collective); a group without rows has no MMAs: its tile is zero
-                const int m = t.mt * BM + row_in_tile;
-                float* dst = nullptr;
-                if (m < p.M)
-                    dst = m < p.split_m
-                              ? p.out_f32 + ((int64_t)t.g * p.split_m + m) * p.N
-                              : p.out_f32b + ((int64_t)t.g * (p.M - p.split_m) + (m - p.split_m)) * p.N;
+                // the warp's 32 rows: all in the first output (rows < split_m) or all in the
+                // second (split_m is a multiple of 32); rows past M are clipped by the map
+                const int m0 = t.mt * BM + q * 32;
+                if (m0 < p.M) {
+                    const bool first = m0 < p.split_m;
+                    const CUtensorMap* map = first ? &tmC0 : &tmC1;
+                    const int32_t row0 = first ? t.g * p.split_m + m0
+                                               : t.g * (p.M - p.split_m) + (m0 - p.split_m);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; c++) {
-                    uint32_t a[32];
-                    if (t.nk > 0) {
-                        tmem_ld32(taddr + c * 32, a);
-                        tmem_ld_wait();
-                    } else {
+                    for (int c = 0; c < BN / 32; c++) {
+                        uint32_t a[32];
+                        if (t.nk > 0) {
+                            tmem_ld32(taddr + c * 32, a);
+                            tmem_ld_wait();
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 32; j++) a[j] = 0u;
+                            for (int j = 0; j < 32; j++) a[j] = 0u;
+                        }
+                        const int col = t.nt * BN + c * 32;
+                        if (col >= p.N) continue;          // warp-uniform
+                        store_chunk_f32(map, sbuf + (uint32_t)(nchunk++ & 1) * STAGE_BUF, a, col, row0);
                     }
-                    const int col = t.nt * BN + c * 32;
-                    if (col >= p.N) continue;              // warp-uniform
-                    store_rows32(buf, a, dst ? reinterpret_cast<uint32_t*>(dst + col) : nullptr,
-                                 min(32, p.N - col));
                 }
             } else {
                 const int rl = t.mt * BM + row_in_tile;          // row within the group
@@ -407,7 +416,9 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         store_rows16(buf, pu, reinterpret_cast<uint32_t*>(p.out_bf16 + pr * p.ld_bf16 + p.F + f));
                         store_rows16(buf, ph, reinterpret_cast<uint32_t*>(p.out2_bf16 + pr * p.F + f));
                     }
-                } else {   // TBE_ROWS_F32: dX rows, fp32
+                } else {   // TBE_ROWS_F32: fp32 rows (padding rows of a segment included; the
+                           // output map clips rows past the buffer)
+                    const int32_t row0 = p.c_off[t.g] + t.mt * BM + q * 32;
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; c++) {
                         uint32_t a[32];
@@ -415,14 +426,14 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         tmem_ld_wait();
                         const int col = t.nt * BN + c * 32;
                         if (col >= p.N) continue;         // warp-uniform
-                        store_rows32(buf, a, valid ? reinterpret_cast<uint32_t*>(p.out_f32 + pr * p.N + col) : nullptr,
-                                     min(32, p.N - col));
+                        store_chunk_f32(&tmC0, sbuf + (uint32_t)(nchunk++ & 1) * STAGE_BUF, a, col, row0);
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
+        if (lane == 0) bulk_wait_all();   // staged stores done before the CTA can exit
         __syncwarp();
     }
 
@@ -437,7 +448,8 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_tb(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const TbParams& p, int64_t max_tiles, cudaStream_t s) {
+                      const CUtensorMap& c0, const CUtensorMap& c1, const TbParams& p,
+                      int64_t max_tiles, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(tcb_kernel<A_MN, B_MN, EPI>,
@@ -447,7 +459,7 @@ cudaError_t launch_tb(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
     }
     const int sms = device_sm_count();
     const int grid = (int)(max_tiles < sms ? (max_tiles < 1 ? 1 : max_tiles) : sms);
-    tcb_kernel<A_MN, B_MN, EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+    tcb_kernel<A_MN, B_MN, EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, c0, c1, p);
     return cudaGetLastError();
 }
 
@@ -464,6 +476,19 @@ bool map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 output [rows, cols], box 32 x 32 (128-byte rows, 128-byte swizzle) for staged stores.
+bool map_f32_store(CUtensorMap* m, const float* base, int64_t rows, int64_t cols) {
+    tc::EncodeTiledFn fn = tc::encode_fn();
+    if (!fn || rows <= 0 || cols <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -483,7 +508,7 @@ cudaError_t tb_dh(const TbParams& p0, const __nv_bfloat16* dout_pad, int64_t row
     p.b_rows = d;
     p.N = F;
     p.n_tiles = tb_dh_tiles(F);
-    return launch_tb<false, true, TBE_DH>(ma, mb, mb, p, p.max_mtiles * (int64_t)p.n_tiles, s);
+    return launch_tb<false, true, TBE_DH>(ma, mb, mb, ma, ma, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
 // G2: recompute gate/up of x_pad, SwiGLU backward with dh_pad; writes [dG | dU] and w * h.
@@ -500,7 +525,7 @@ cudaError_t tb_swiglu_bwd(const TbParams& p0, const __nv_bfloat16* x_pad, int64_
     p.b_rows = F;
     p.F = F;
     p.n_tiles = F / (BN / 2);
-    return launch_tb<false, false, TBE_SWIGLU_BWD>(ma, mg, mu, p, p.max_mtiles * (int64_t)p.n_tiles, s);
+    return launch_tb<false, false, TBE_SWIGLU_BWD>(ma, mg, mu, ma, ma, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
 // G3: dX = [dG | dU] . [W_g; W_u] (fp32 rows).  dgu [rows_a, 2F], W_g, W_u [G*F, d].
@@ -510,6 +535,8 @@ cudaError_t tb_dx(const TbParams& p0, const __nv_bfloat16* dgu, int64_t rows_a, 
     if (!map_bf16(&ma, dgu, rows_a, 2 * F, 64, BM) || !map_bf16(&mg, Wg, (int64_t)p0.G * F, d, 64, 64) ||
         !map_bf16(&mu, Wu, (int64_t)p0.G * F, d, 64, 64))
         return cudaErrorInvalidValue;
+    CUtensorMap mc;
+    if (!map_f32_store(&mc, p0.out_f32, rows_a, d)) return cudaErrorInvalidValue;
     TbParams p = p0;
     p.mode = TB_ROWS;
     p.K = 2 * F;
@@ -517,15 +544,16 @@ cudaError_t tb_dx(const TbParams& p0, const __nv_bfloat16* dgu, int64_t rows_a, 
     p.b_rows = F;
     p.N = d;
     p.n_tiles = (d + BN - 1) / BN;
-    return launch_tb<false, true, TBE_ROWS_F32>(ma, mg, mu, p, p.max_mtiles * (int64_t)p.n_tiles, s);
+    return launch_tb<false, true, TBE_ROWS_F32>(ma, mg, mu, mc, mc, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
 // Rows GEMM of one operand pair: out[r, :] (fp32) = A[a_off + r, :K] (K-major) . B[k, :N]
 // (B [K rows, N], MN-major), for the group rows given in p (the router's part of dx).
 cudaError_t tb_rows_f32(const TbParams& p0, const __nv_bfloat16* A, int64_t rows_a, int K,
                         const __nv_bfloat16* B, int N, cudaStream_t s) {
-    CUtensorMap ma, mb;
-    if (!map_bf16(&ma, A, rows_a, K, 64, BM) || !map_bf16(&mb, B, K, N, 64, 64))
+    CUtensorMap ma, mb, mc;
+    if (!map_bf16(&ma, A, rows_a, K, 64, BM) || !map_bf16(&mb, B, K, N, 64, 64) ||
+        !map_f32_store(&mc, p0.out_f32, rows_a, N))
         return cudaErrorInvalidValue;
     TbParams p = p0;
     p.mode = TB_ROWS;
@@ -534,7 +562,7 @@ cudaError_t tb_rows_f32(const TbParams& p0, const __nv_bfloat16* A, int64_t rows
     p.b_rows = 0;
     p.N = N;
     p.n_tiles = (N + BN - 1) / BN;
-    return launch_tb<false, true, TBE_ROWS_F32>(ma, mb, mb, p, p.max_mtiles * (int64_t)p.n_tiles, s);
+    return launch_tb<false, true, TBE_ROWS_F32>(ma, mb, mb, mc, mc, p, p.max_mtiles * (int64_t)p.n_tiles, s);
 }
 
 // Weight gradients: out[g] (M x N fp32, rows < split_m into out_f32, the rest into out_f32b)
@@ -545,13 +573,19 @@ cudaError_t tb_wgrad(const TbParams& p0, const __nv_bfloat16* A, int64_t rows_a,
     CUtensorMap ma, mb;
     if (!map_bf16(&ma, A, rows_a, a_cols > 0 ? a_cols : M, 64, 64) || !map_bf16(&mb, B, rows_b, N, 64, 64))
         return cudaErrorInvalidValue;
+    // outputs: rows [0, split_m) of every group in out_f32, the rest in out_f32b
+    CUtensorMap c0, c1;
+    const int m1 = M - p0.split_m;
+    if (!map_f32_store(&c0, p0.out_f32, (int64_t)p0.G * p0.split_m, N) ||
+        !map_f32_store(&c1, p0.out_f32b, (int64_t)p0.G * (m1 > 0 ? m1 : p0.split_m), N))
+        return cudaErrorInvalidValue;
     TbParams p = p0;
     p.mode = TB_WEIGHTS;
     p.M = M;
     p.N = N;
     p.m_tiles = (M + BM - 1) / BM;
     p.n_tiles = (N + BN - 1) / BN;
-    return launch_tb<true, true, TBE_F32>(ma, mb, mb, p, (int64_t)p.G * p.m_tiles * p.n_tiles, s);
+    return launch_tb<true, true, TBE_F32>(ma, mb, mb, c0, c1, p, (int64_t)p.G * p.m_tiles * p.n_tiles, s);
 }
 
 // One group, any operand majorness, fp32 out: the engine's self-test (see selftest.cu).
@@ -578,11 +612,13 @@ cudaError_t tb_selftest(bool a_mn, bool b_mn, int M, int N, int K, const __nv_bf
     const bool okA = a_mn ? map_bf16(&ma, A, K, M, 64, 64) : map_bf16(&ma, A, M, K, 64, BM);
     const bool okB = b_mn ? map_bf16(&mb, B, K, N, 64, 64) : map_bf16(&mb, B, N, K, 64, BN);
     if (!okA || !okB) return cudaErrorInvalidValue;
+    CUtensorMap mc;
+    if (!map_f32_store(&mc, C, M, N)) return cudaErrorInvalidValue;
     const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-    if (a_mn && b_mn) return launch_tb<true, true, TBE_F32>(ma, mb, mb, p, tiles, s);
-    if (a_mn) return launch_tb<true, false, TBE_F32>(ma, mb, mb, p, tiles, s);
-    if (b_mn) return launch_tb<false, true, TBE_F32>(ma, mb, mb, p, tiles, s);
-    return launch_tb<false, false, TBE_F32>(ma, mb, mb, p, tiles, s);
+    if (a_mn && b_mn) return launch_tb<true, true, TBE_F32>(ma, mb, mb, mc, mc, p, tiles, s);
+    if (a_mn) return launch_tb<true, false, TBE_F32>(ma, mb, mb, mc, mc, p, tiles, s);
+    if (b_mn) return launch_tb<false, true, TBE_F32>(ma, mb, mb, mc, mc, p, tiles, s);
+    return launch_tb<false, false, TBE_F32>(ma, mb, mb, mc, mc, p, tiles, s);
 }
 
 }  // namespace moe
