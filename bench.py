@@ -6,8 +6,9 @@ A step is one moe_forward (router, permute, grouped gate/up and down GEMMs, shar
 combine) over one resident batch of the named workload; the default workload is the
 Mixtral-shaped bf16 layer (N=4096, d=4096, d_ff=14336, E=8, top-2).  Weights (2.8 GB) exceed the
 126 MB L2, so no flush is needed between steps.  `value` is tokens/s over all ranks from CUDA
-events; `e2e` repeats the measurement through the same C ABI with the batch copied in from pinned
-host memory and the output copied back every step.  `roofline` reports the dominant kernel (the
+events; `e2e` repeats the measurement through the same C ABI with every step's batch copied in
+from pinned host memory and its output copied back (the copies on their own streams, double
+buffered, overlapping the neighbouring steps' layers).  `roofline` reports the dominant kernel (the
 routed gate/up grouped GEMM) against the measured bf16 peak.  `cpu_baseline` times the CPU oracle
 on a bounded sub-batch of the same layer.  Under torchrun (N > 1) every rank runs its own replica
 (the layer needs no exchange between GPUs).  The W4A16 workload runs moe_forward_w4a16 on expert
@@ -304,21 +305,46 @@ def main():
     phase_roof = phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks)
 
     # ---------------- end to end through the C ABI with host buffers
+    # Every step copies its batch in from pinned host memory and its output back.  The copies run
+    # on their own streams with two device buffers each way, so step i's upload and step i-2's
+    # download overlap step i-1's layer (events keep each buffer's uses in order).
     x_host = [x.cpu().pin_memory() for x in xs]
-    out_host = torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory()
-    x_dev = torch.empty_like(xs[0])
+    out_host = [torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(xs[0]) for _ in range(2)]
+    out_dev = [torch.empty_like(lay.out) for _ in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     e2e_steps = max(3, min(args.steps, 50))
-    for i in range(3):
-        x_dev.copy_(x_host[i % 2], non_blocking=True)
-        out_host.copy_(lay.forward(x_dev), non_blocking=True)
+
+    def run_e2e(n):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        ev_d2h = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(ev_out[i - 2])          # x_dev[b] read by step i-2
+                x_dev[b].copy_(x_host[i % 2], non_blocking=True)
+                ev_in[i].record(up)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_d2h[i - 2])          # out_dev[b] copied out by step i-2
+            lay.forward(x_dev[b], out=out_dev[b])
+            ev_out[i].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_out[i])
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+                ev_d2h[i].record(down)
+        return ev_d2h[n - 1]
+
+    run_e2e(3)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        x_dev.copy_(x_host[i % 2], non_blocking=True)
-        out_host.copy_(lay.forward(x_dev), non_blocking=True)
-    e1.record(stream)
+    e0.record(up)
+    last = run_e2e(e2e_steps)
+    down.wait_event(last)
+    e1.record(down)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:

@@ -408,17 +408,20 @@ class MoELayer:
         act = torch.bfloat16 if cfg.act_dtype == MOE_BF16 else torch.float32
         self.out = torch.empty((cfg.N, cfg.d), dtype=act, device=self.device)
 
-    def forward(self, x: torch.Tensor, stream=None, events=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, stream=None, events=None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """out: where to write the layer output (default: the layer's own buffer)."""
         w = self.w
         self.last_x = x
+        out = self.out if out is None else out
         if self.w4 is not None:
-            moe_forward_w4a16(self.cfg, x, w["W_r"], w.get("b_r"), self.w4, self.out, self.ws,
+            moe_forward_w4a16(self.cfg, x, w["W_r"], w.get("b_r"), self.w4, out, self.ws,
                               stream, events)
-            return self.out
+            return out
         moe_forward(self.cfg, x, w["W_r"], w.get("b_r"), w["W_gate"], w["W_up"], w["W_down"],
-                    w.get("Ws_gate"), w.get("Ws_up"), w.get("Ws_down"), self.out, self.ws,
+                    w.get("Ws_gate"), w.get("Ws_up"), w.get("Ws_down"), out, self.ws,
                     stream, events)
-        return self.out
+        return out
 
     def buffers(self) -> dict:
         return moe_forward_buffers(self.cfg, self.ws)
