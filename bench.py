@@ -179,6 +179,25 @@ def _oracle_w4_batch(spec, L) -> float:
     return t_route + time.perf_counter() - t0
 
 
+# ------------------------------------------------------------------ several ranks (replicas)
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank runs its own replica over its own batch, and the job
+    is done when the last one is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: the tokens of all ranks over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def metric_name(spec) -> str:
     if spec == moe_synth.MIXTRAL:
         return "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
@@ -275,15 +294,11 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
     if lay.device_error() != 0:
         raise RuntimeError("device error during the timed region")
     ms_step = elapsed_ms / args.steps
-    value = spec.N * world / (ms_step / 1e3)
+    value = job_rate(spec.N, world, ms_step)
 
     phases = ["route", "permute", "gateup", "down", "shared", "combine"]
     ph_ms = {p: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
@@ -346,12 +361,8 @@ def main():
     down.wait_event(last)
     e1.record(down)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = spec.N * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, "cuda")
+    e2e_value = job_rate(spec.N, world, e2e_ms)
 
     # router 2, permute 4, m-tile plan 1 (not on the W4A16 path), routed 2, shared 2, combine 1
     # ---------------- backward pass (bf16 layers whose fp32 weight gradients fit comfortably)
