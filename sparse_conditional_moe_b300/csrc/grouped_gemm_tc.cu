@@ -21,6 +21,10 @@
 // yields both projections of 128 hidden units side by side in TMEM.
 // Tiles are ordered group-major, then n-tile, with the m-tiles of a group innermost, so the
 // CTAs working at the same time share a weight tile through L2.
+// The last m-tile of a group is usually ragged (a group of 257 rows needs a third tile for one
+// row).  When it holds at most kSwapMaxRows rows it is computed transposed: the same shared
+// memory stages feed two MMAs with the weight rows as M = 128 and the tile's rows, rounded up to
+// 16, as N, and the epilogue writes the transposed accumulator (lane = output column).
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises an abort flag, the
 // other roles stop at their next wait, in-flight copies and MMAs are drained with bounded
 // waits, TMEM is freed and the device error word gets MOE_DEVERR_TIMEOUT.
@@ -32,8 +36,8 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BK = 64, BN = 256, STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;
-constexpr int B_STAGE = BN * BK * 2;
+constexpr int A_STAGE = BM * BK * 2;      // 16 KB: 128 rows of A
+constexpr int B_STAGE = BN * BK * 2;      // 32 KB: 256 rows of B
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
@@ -61,9 +65,18 @@ struct TcParams {
 
 // ---------------------------------------------------------------- tile scheduling
 
+// The last m-tile of a group is usually ragged (a group of 257 rows needs a third tile for one
+// row).  When it holds at most kSwapMaxRows rows it is computed with the operands swapped: the
+// weight rows are the MMA's M = 128 side (two MMAs: gate and up, or the two 128-row halves of
+// the down tile) and the tile's rows are its N side, rounded up to 16, so the MMA work shrinks
+// with the rows present.
+constexpr int kSwapMaxRows = 96;
+
 struct TileInfo {
     int g, mt, nt, rows;
     int64_t a_row0, c_row0;
+    int tr;       // valid rows of this m-tile (1..BM)
+    bool swap;    // computed with the operands swapped (tr <= kSwapMaxRows)
 };
 
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
@@ -98,6 +111,9 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int tile) {
         t.rows = p.rows[lo];
         t.a_row0 = t.c_row0 = p.row_off[lo];
     }
+    const int left = t.rows - t.mt * BM;
+    t.tr = left < BM ? left : BM;
+    t.swap = t.tr <= kSwapMaxRows;
     return t;
 }
 
@@ -106,6 +122,104 @@ __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- epilogues (one warp each)
+
+// Accumulator of rows in TMEM lanes: rows [row0 + q*32, +32) of the part, all 256 columns.
+template <int EPI>
+__device__ __forceinline__ void epi_rows(const TcParams& p, const CUtensorMap* tmC, uint32_t taddr,
+                                         uint32_t stage0, int& nchunk, int q, int nt, int64_t row0,
+                                         int nrows) {
+    const int lane = threadIdx.x & 31;
+    const int r = q * 32 + lane;
+    const bool valid = r < nrows;
+    const bool all_valid = q * 32 + 31 < nrows;   // warp-uniform
+    const int64_t crow = row0 + r;
+    const int32_t gy = (int32_t)(row0 + q * 32);
+    if (EPI == EPI_SWIGLU) {
+        const int col0 = nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < (BN / 2) / 32; c++, nchunk++) {
+            uint32_t g[32], u[32];
+            tmem_ld32(taddr + c * 32, g);
+            tmem_ld32(taddr + BN / 2 + c * 32, u);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                pk[j] = pack_bf16(h0, h1);
+            }
+            const int col = col0 + c * 32;
+            store_chunk32(tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
+                          p.C + crow * p.ldc + col, col, p.n_out, gy);
+        }
+    } else {
+        const int col0 = nt * BN;
+        const float sc = (valid && p.row_scale) ? p.row_scale[crow] : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c++, nchunk++) {
+            uint32_t a[32];
+            tmem_ld32(taddr + c * 32, a);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                pk[j] = pack_bf16(__uint_as_float(a[2 * j]) * sc, __uint_as_float(a[2 * j + 1]) * sc);
+            const int col = col0 + c * 32;
+            store_chunk32(tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
+                          p.C + crow * p.ldc + col, col, p.n_out, gy);
+        }
+    }
+}
+
+// Swapped accumulator: TMEM lane = output column (this warp: 32 of them), TMEM column = row;
+// columns [0, n16) hold the first 128 weight rows, [128, 128 + n16) the second 128.
+template <int EPI>
+__device__ __forceinline__ void epi_swapped(const TcParams& p, const CUtensorMap* tmC,
+                                            uint32_t taddr, uint32_t stage0, int& nchunk, int q,
+                                            int nt, int64_t row0, int nrows) {
+    const int lane = threadIdx.x & 31;
+    const int nch = (nrows + 31) >> 5;
+    if (EPI == EPI_SWIGLU) {
+        const int col = nt * (BN / 2) + q * 32;
+        const bool col_ok = col + lane < p.n_out;
+#pragma unroll 1
+        for (int c = 0; c < nch; c++, nchunk++) {
+            uint32_t g[32], u[32];
+            tmem_ld32(taddr + c * 32, g);
+            tmem_ld32(taddr + BN / 2 + c * 32, u);
+            tmem_ld_wait();
+            float h[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) h[j] = silu(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+            const int64_t gr = row0 + c * 32;
+            store_chunk32_t(tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, h, nrows - c * 32,
+                            p.C + gr * p.ldc + col + lane, p.ldc, col_ok, col, (int32_t)gr);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < nch; c++) {
+            const int64_t gr = row0 + c * 32;
+            const float s_lane = (p.row_scale && c * 32 + lane < nrows) ? p.row_scale[gr + lane] : 1.f;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; hh++, nchunk++) {
+                uint32_t a[32];
+                tmem_ld32(taddr + hh * (BN / 2) + c * 32, a);
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++)
+                    v[j] = __uint_as_float(a[j]) * __shfl_sync(0xffffffffu, s_lane, j);
+                const int col = nt * BN + hh * (BN / 2) + q * 32;
+                store_chunk32_t(tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, v, nrows - c * 32,
+                                p.C + gr * p.ldc + col + lane, p.ldc, col + lane < p.n_out, col,
+                                (int32_t)gr);
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -118,8 +232,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_STAGE;
+    uint8_t* sA = smem;                          // [STAGES] x 16 KB
+    uint8_t* sB = smem + STAGES * A_STAGE;       // [STAGES] x 32 KB
     uint8_t* sStage = smem + STAGES * STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGING_BYTES);
     uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
@@ -206,6 +320,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
+            // Kept lean (its issue rate shows in the tensor pipe's utilisation): one k-loop per
+            // tile kind, descriptors advanced by addition (+2 = 32 bytes = K 16).
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
             int s = 0;
             uint32_t ph = 0;
@@ -220,18 +336,31 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const TileInfo t = decode_tile(p, tile);
+                // swapped: D0 = W[0:128) . A^T and D1 = W[128:256) . A^T, each 128 x n16
+                const uint32_t idesc_sw = idesc_bf16_f32(BM, (t.tr + 15) & ~15);
                 for (int kb = 0; kb < nk; kb++) {
                     if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + s * A_STAGE);
-                    const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+                    const uint64_t ad = sw128_desc(smem_u32(sA + s * A_STAGE));
+                    const uint64_t bd = sw128_desc(smem_u32(sB + s * B_STAGE));
+                    if (!t.swap) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; kk++)
-                        umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / 16; kk++)
+                            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
+                                      (kb > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint64_t bd_hi = bd + (uint64_t)((B_STAGE / 2) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; kk++) {
+                            const uint32_t acc_in = (kb > 0 || kk > 0) ? 1u : 0u;
+                            umma_bf16(d_tmem, bd + 2 * kk, ad + 2 * kk, idesc_sw, acc_in);
+                            umma_bf16(d_tmem + BN / 2, bd_hi + 2 * kk, ad + 2 * kk, idesc_sw, acc_in);
+                        }
+                    }
                     umma_commit(&empty[s]);
                     if (++s == STAGES) {
                         s = 0;
@@ -248,60 +377,20 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else {
         // ---------------------------------------------------- epilogue (warps 2..5)
         const int q = warp & 3;   // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
         const uint32_t stage0 = smem_u32(sStage) + (uint32_t)(warp - 2) * 4096u;
         int nchunk = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            if (!waitw(&tfull[acc], aph, abort_flag)) break;
+            if (!waitw(&tfull[acc], (uint32_t)(it >> 1) & 1u, abort_flag)) break;
             tc_fence_after();
             const TileInfo t = decode_tile(p, tile);
-            const int r = t.mt * BM + row_in_tile;
-            const bool valid = r < t.rows;
-            const bool all_valid = t.mt * BM + q * 32 + 31 < t.rows;   // warp-uniform
-            const int64_t crow = t.c_row0 + r;
-            const int32_t gy = (int32_t)(t.c_row0 + t.mt * BM + q * 32);
+            const int64_t row0 = t.c_row0 + (int64_t)t.mt * BM;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (EPI == EPI_SWIGLU) {
-                const int col0 = t.nt * (BN / 2);
-#pragma unroll 1
-                for (int c = 0; c < (BN / 2) / 32; c++, nchunk++) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(taddr + c * 32, g);
-                    tmem_ld32(taddr + BN / 2 + c * 32, u);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                        const float h1 =
-                            silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-                        pk[j] = pack_bf16(h0, h1);
-                    }
-                    const int col = col0 + c * 32;
-                    store_chunk32(&tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
-                                  p.C + crow * p.ldc + col, col, p.n_out, gy);
-                }
-            } else {
-                const int col0 = t.nt * BN;
-                const float sc = (valid && p.row_scale) ? p.row_scale[crow] : 1.f;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c++, nchunk++) {
-                    uint32_t a[32];
-                    tmem_ld32(taddr + c * 32, a);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        pk[j] = pack_bf16(__uint_as_float(a[2 * j]) * sc,
-                                          __uint_as_float(a[2 * j + 1]) * sc);
-                    const int col = col0 + c * 32;
-                    store_chunk32(&tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, pk, all_valid, valid,
-                                  p.C + crow * p.ldc + col, col, p.n_out, gy);
-                }
-            }
+            if (t.swap)
+                epi_swapped<EPI>(p, &tmC, taddr, stage0, nchunk, q, t.nt, row0, t.tr);
+            else
+                epi_rows<EPI>(p, &tmC, taddr, stage0, nchunk, q, t.nt, row0, t.tr);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }

@@ -202,6 +202,43 @@ static __device__ __forceinline__ void store_chunk32(const CUtensorMap* tmC, uin
     }
 }
 
+static __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Transposed form of store_chunk32 for tiles computed with the operands swapped: lane = output
+// column (col + lane), v[j] = the value of row gy + j.  The warp writes the same 32 x 32 block
+// as store_chunk32: whole (nrows >= 32) through the staging buffer in its 64-byte-swizzled
+// layout and one TMA store, otherwise the first nrows rows with 2-byte stores (a warp covers
+// 64 contiguous bytes of one row per store); col_ok says whether this lane's column is < n_out.
+static __device__ __forceinline__ void store_chunk32_t(const CUtensorMap* tmC, uint32_t buf,
+                                                       const float (&v)[32], int nrows,
+                                                       __nv_bfloat16* dst, int64_t ldc, bool col_ok,
+                                                       int col, int32_t gy) {
+    const int lane = threadIdx.x & 31;
+    if (nrows >= 32) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t ch = (uint32_t)lane >> 3, cb = ((uint32_t)lane & 7u) * 2u;
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(v[j]);
+            st_shared_u16(buf + (uint32_t)j * 64u + ((ch ^ (((uint32_t)j >> 1) & 3u)) << 4) + cb,
+                          *reinterpret_cast<const uint16_t*>(&b));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d_hint(tmC, buf, col, gy, policy_evict_first());
+            bulk_commit();
+        }
+    } else if (col_ok) {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+            if (j < nrows) dst[(int64_t)j * ldc] = __float2bfloat16_rn(v[j]);
+    }
+}
+
 // ---------------------------------------------------------------- tile order inside a group
 
 // Tile `local` of a group with mtg m-tiles and nt n-tiles -> (m-tile, n-tile).  m-tiles run in
