@@ -316,7 +316,7 @@ def main():
     layer_tflops = work.flops / (ms_step / 1e3) / 1e12
     layer_gbs = work.bytes / (ms_step / 1e3) / 1e9
     roof_s = work.roofline_s(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-    traffic = read_traffic("gateup")
+    traffic = read_traffic("gateup", spec.name)
     phase_roof = phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks)
 
     # ---------------- end to end through the C ABI with host buffers
@@ -484,19 +484,21 @@ def phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks):
     return out
 
 
-def read_traffic(kernel: str):
+def read_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if its source hash is current."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", "grouped_gemm_tc.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in ("grouped_gemm_tc.cu", "tc_ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", f), "rb").read())
+    h = h.hexdigest()[:16]
     for ln in open(path):
         parts = [p.strip() for p in ln.strip().strip("|").split("|")]
-        if len(parts) >= 4 and parts[0] == kernel and parts[1] == h:
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == h:
             try:
-                return float(parts[2])
+                return float(parts[3])
             except ValueError:
                 return None
     return None

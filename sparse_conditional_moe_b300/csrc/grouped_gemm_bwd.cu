@@ -274,14 +274,17 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         break;
                     }
                     tc_fence_after();
+                    // descriptors advance by addition: K 16 = 32 bytes (K-major) or 2048 bytes
+                    // (MN-major), i.e. +2 or +128 in the address field
                     const uint32_t a0 = smem_u32(sA + s * A_STAGE);
                     const uint32_t b0 = smem_u32(sB + s * B_STAGE);
+                    const uint64_t ad = A_MN ? sw128_mn_desc(a0) : sw128_desc(a0);
+                    const uint64_t bd = B_MN ? sw128_mn_desc(b0) : sw128_desc(b0);
+                    constexpr uint64_t a_step = A_MN ? 128 : 2, b_step = B_MN ? 128 : 2;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; kk++) {
-                        const uint64_t ad = A_MN ? sw128_mn_desc(a0 + kk * 2048) : sw128_desc(a0 + kk * 32);
-                        const uint64_t bd = B_MN ? sw128_mn_desc(b0 + kk * 2048) : sw128_desc(b0 + kk * 32);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / 16; kk++)
+                        umma_bf16(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);
                     if (++s == STAGES) {
                         s = 0;

@@ -253,7 +253,7 @@ router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
 
 // ------------------------------------------------------------------ logits -> top-k
 
-constexpr int kTopkTokensPerBlock = 32;
+constexpr int kTopkTokensPerBlock = 8;   // one token per warp: latency is hidden by occupancy
 
 template <int NV>
 __global__ void __launch_bounds__(kRouterThreads)
@@ -391,18 +391,33 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
     write_p_part<NV>(pacc, sm, E, p_part);
 }
 
-// P_sum[e] = sum over router blocks of p_part[b][e]: one warp per expert, lanes take every
-// 32nd block, fixed butterfly (deterministic).
-__global__ void reduce_p_kernel(const float* __restrict__ p_part, int blocks, int E,
-                                float* __restrict__ P_sum) {
-    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (e >= E) return;
+// P_sum[e] = sum over router blocks b of p_part[b][e], in a fixed order (deterministic): one
+// block of 32 warps per 32 experts, lane = expert (coalesced rows); warp w adds blocks w, w + 32,
+// ... in order with eight loads in flight, then warp 0 adds the 32 warp sums in warp order.
+__global__ void __launch_bounds__(1024) reduce_p_kernel(const float* __restrict__ p_part, int blocks,
+                                                        int E, float* __restrict__ P_sum) {
+    __shared__ float part[32][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
     float s = 0.f;
-    for (int b = lane; b < blocks; b += 32) s += p_part[(int64_t)b * E + e];
+    if (e < E) {
+        int b = warp;
+        for (; b + 7 * 32 < blocks; b += 8 * 32) {
+            float v[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) P_sum[e] = s;
+            for (int i = 0; i < 8; i++) v[i] = p_part[(int64_t)(b + 32 * i) * E + e];
+#pragma unroll
+            for (int i = 0; i < 8; i++) s += v[i];
+        }
+        for (; b < blocks; b += 32) s += p_part[(int64_t)b * E + e];
+    }
+    part[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && e < E) {
+        float t = 0.f;
+        for (int w = 0; w < 32; w++) t += part[w][lane];
+        P_sum[e] = t;
+    }
 }
 
 int pad_experts(int E) {
@@ -491,7 +506,7 @@ cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, con
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    reduce_p_kernel<<<(c.E + 7) / 8, 256, 0, s>>>(p_part, blocks, c.E, P_sum);
+    reduce_p_kernel<<<(c.E + 31) / 32, 1024, 0, s>>>(p_part, blocks, c.E, P_sum);
     return cudaGetLastError();
 }
 
