@@ -54,17 +54,27 @@ struct Vec<float> {
     }
 };
 
-// One warp per token, lanes over 16-byte column chunks.
+// A warp takes one (token, column segment) unit at a time, lanes over 16-byte vectors, two
+// vectors per lane per pass (2 (k + S) independent loads in flight).  Large batches use one
+// segment per token (the whole row); a decode batch of a few dozen tokens splits each row into
+// `segs` segments so that enough warps run to cover the memory latency.
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T* __restrict__ ysh,
-               int S, int64_t N, int d, int k, int64_t R, T* __restrict__ out, int32_t* err) {
+               int S, int64_t N, int d, int k, int64_t R, int segs, T* __restrict__ out,
+               int32_t* err) {
     constexpr int V = Vec<T>::N;
     const int lane = threadIdx.x & 31;
     const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int chunks = d / V;
-    for (int64_t t = warp_global; t < N; t += warps) {
+    const int span = ((chunks + segs - 1) / segs + 63) / 64 * 64;   // vectors per segment
+    const int64_t units = N * segs;   // < 2^32 (checked by the host)
+    for (int64_t u = warp_global; u < units; u += warps) {
+        const uint32_t t32 = (uint32_t)u / (uint32_t)segs;
+        const int sg = (int)((uint32_t)u - t32 * (uint32_t)segs);
+        const int64_t t = t32;
+        const int c_end = min(chunks, (sg + 1) * span);
         int32_t p[16];
 #pragma unroll
         for (int j = 0; j < 16; j++) {
@@ -72,14 +82,14 @@ combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T
             if (j < k) {
                 int32_t v = pos[t * k + j];
                 if (v >= R) {
-                    if (lane == 0) atomicOr(err, MOE_DEVERR_BOUNDS);
+                    if (lane == 0 && sg == 0) atomicOr(err, MOE_DEVERR_BOUNDS);
                     v = -1;
                 }
                 p[j] = v;
             }
         }
-        int c = lane;
-        for (; c + 32 < chunks; c += 64) {   // two column chunks per pass: 2(k+S) loads in flight
+        int c = sg * span + lane;
+        for (; c + 32 < c_end; c += 64) {   // two vectors per pass
             float a[V], b[V];
 #pragma unroll
             for (int i = 0; i < V; i++) a[i] = b[i] = 0.f;
@@ -89,21 +99,21 @@ combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T
                     Vec<T>::add(y + (int64_t)p[j] * d + c * V, a);
                     Vec<T>::add(y + (int64_t)p[j] * d + (c + 32) * V, b);
                 }
-            for (int s = 0; s < S; s++) {
-                Vec<T>::add(ysh + ((int64_t)s * N + t) * d + c * V, a);
-                Vec<T>::add(ysh + ((int64_t)s * N + t) * d + (c + 32) * V, b);
+            for (int s2 = 0; s2 < S; s2++) {
+                Vec<T>::add(ysh + ((int64_t)s2 * N + t) * d + c * V, a);
+                Vec<T>::add(ysh + ((int64_t)s2 * N + t) * d + (c + 32) * V, b);
             }
             Vec<T>::store(out + t * d + c * V, a);
             Vec<T>::store(out + t * d + (c + 32) * V, b);
         }
-        for (; c < chunks; c += 32) {
+        for (; c < c_end; c += 32) {
             float a[V];
 #pragma unroll
             for (int i = 0; i < V; i++) a[i] = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; j++)
                 if (j < k && p[j] >= 0) Vec<T>::add(y + (int64_t)p[j] * d + c * V, a);
-            for (int s = 0; s < S; s++) Vec<T>::add(ysh + ((int64_t)s * N + t) * d + c * V, a);
+            for (int s2 = 0; s2 < S; s2++) Vec<T>::add(ysh + ((int64_t)s2 * N + t) * d + c * V, a);
             Vec<T>::store(out + t * d + c * V, a);
         }
     }
@@ -305,15 +315,25 @@ cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* 
                            const void* y_sh, void* out, int32_t* err, cudaStream_t s) {
     if (c.N <= 0) return cudaSuccess;
     const int64_t R = grouped_rows(c);
-    int64_t want = (c.N + 7) / 8;
-    int blocks = (int)(want < 148 * 16 ? want : 148 * 16);
+    // segments per token: 1 for large batches, more when N warps cannot cover the GPU
+    const int vec = c.act_dtype == MOE_BF16 ? 8 : 4;
+    const int64_t resident = (int64_t)device_sm_count() * 64;   // warps the GPU holds at once
+    const int max_segs = (int)(((int64_t)c.d / vec + 63) / 64);
+    int64_t segs = (resident + c.N - 1) / c.N;
+    if (segs > max_segs) segs = max_segs;
+    if (segs < 1) segs = 1;
+    if (c.N * segs >= (int64_t)1 << 32) return cudaErrorInvalidValue;
+    const int64_t want = (c.N * segs + 7) / 8;   // 8 warps per block
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    const int blocks = (int)(want < cap ? want : cap);
     if (c.act_dtype == MOE_BF16)
         combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
             (const __nv_bfloat16*)y_perm, pos, (const __nv_bfloat16*)y_sh, c.n_shared, c.N, c.d,
-            c.k, R, (__nv_bfloat16*)out, err);
+            c.k, R, (int)segs, (__nv_bfloat16*)out, err);
     else
         combine_kernel<float><<<blocks, 256, 0, s>>>((const float*)y_perm, pos, (const float*)y_sh,
-                                                     c.n_shared, c.N, c.d, c.k, R, (float*)out, err);
+                                                     c.n_shared, c.N, c.d, c.k, R, (int)segs,
+                                                     (float*)out, err);
     return cudaGetLastError();
 }
 

@@ -64,7 +64,7 @@ WsLayout ws_layout(const moe_cfg& c) {
     L.p_part = take(4 * (size_t)router_part_rows(N) * E);
     const bool tc_router = router_uses_tensor_cores(c);
     L.router_w3 = take(tc_router ? 2 * 3 * (size_t)E * d : 0);
-    L.logits = take(tc_router ? 4 * (size_t)N * E : 0);
+    L.logits = take(tc_router ? 4 * router_tc_logits_floats(N, (int)d, (int)E) : 0);
     L.blk_hist = take(4 * (size_t)perm_blocks(A) * E);
     L.blk_base = take(4 * (size_t)perm_blocks(A) * E);
     L.mtile_off = take(4 * (size_t)(E + 1));

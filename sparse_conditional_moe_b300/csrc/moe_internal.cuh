@@ -59,6 +59,10 @@ cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, con
                           cudaStream_t s, float* probs = nullptr);
 
 // Tensor-core router logits [N, E] (fp32) for bf16 x (see router_tc.cu).
+// Tensor-core router: number of CTA groups that split d (1 = none; small N only) and the floats
+// its logits region needs (the logits, plus one [N, E] slice sum per 256 of d when split).
+int router_tc_split(int64_t N, int d, int E);
+size_t router_tc_logits_floats(int64_t N, int d, int E);
 cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
                              __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s);
 

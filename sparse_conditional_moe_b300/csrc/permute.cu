@@ -203,6 +203,13 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_
         const uint4* src = x + t * row_vecs;
         uint4* dst = xp + r * row_vecs;
         int v = lane;
+        for (; v + 224 < row_vecs; v += 256) {   // eight 16-byte loads in flight per lane
+            uint4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) a[i] = __ldg(src + v + 32 * i);
+#pragma unroll
+            for (int i = 0; i < 8; i++) dst[v + 32 * i] = a[i];
+        }
         for (; v + 96 < row_vecs; v += 128) {   // four 16-byte loads in flight per lane
             const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
                         e = __ldg(src + v + 96);

@@ -33,17 +33,24 @@ __device__ __forceinline__ float load_x(const __nv_bfloat16* x, int64_t i) {
     return __bfloat162float(x[i]);
 }
 
-// Warp arg-max over (value desc, index asc); every lane ends with the same pair.
+// Unsigned key with the order of the float (negative floats bit-flipped, -0 made +0); a NaN
+// gets the lowest key, so like the comparisons it stands for it never wins over a number.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const float f = v == 0.f ? 0.f : v;
+    const uint32_t u = __float_as_uint(f);
+    return (f != f) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Warp arg-max over (value desc, index asc); every lane ends with the same pair: the maximum key
+// is one warp reduction and the lowest index among the lanes holding it a second.
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        int oi = __shfl_xor_sync(0xffffffffu, i, off);
-        if (ov > v || (ov == v && oi < i)) {
-            v = ov;
-            i = oi;
-        }
-    }
+    const uint32_t key = order_key(v);
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+    i = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)i : 0xffffffffu);
+    v = key_value(mk);
 }
 
 // Softmax, top-k, gap and renormalisation of one token held by one warp.  v[i] is the logit of
@@ -95,10 +102,63 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
         const int e = lane + 32 * i;
         sv[i] = (bias_mode == 2 && e < E) ? v[i] + b_r[e] : v[i];
     }
-    uint32_t taken = 0;
     float my_val = 0.f, kth = 0.f, sel_sum = 0.f;
     int my_idx = 0;
     const int rounds = k < E ? k + 1 : k;
+    if constexpr (NV <= 8) {
+        // Each lane sorts its NV candidates once by (score desc, expert asc); every round the
+        // lanes offer their heads, two warp reductions pick the winner (the same order as a
+        // full arg-max over the untaken experts) and the winning lane pops its head.
+        uint32_t key[NV];
+        int ex[NV];
+        float pr[NV];
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int e = lane + 32 * i;
+            key[i] = e < E ? order_key(sv[i]) : 0u;
+            ex[i] = e < E ? e : INT_MAX;
+            pr[i] = v[i];
+        }
+#pragma unroll
+        for (int a = 1; a < NV; a++)
+#pragma unroll
+            for (int b = a; b > 0; b--)
+                if (key[b] > key[b - 1]) {   // strict: equal keys keep the lower expert first
+                    const uint32_t tk = key[b]; key[b] = key[b - 1]; key[b - 1] = tk;
+                    const int te = ex[b]; ex[b] = ex[b - 1]; ex[b - 1] = te;
+                    const float tp = pr[b]; pr[b] = pr[b - 1]; pr[b - 1] = tp;
+                }
+        for (int j = 0; j < rounds; j++) {
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, key[0]);
+            const int bi =
+                (int)__reduce_min_sync(0xffffffffu, key[0] == mk ? (uint32_t)ex[0] : 0xffffffffu);
+            const float bv = key_value(mk);
+            if (j < k) {
+                const int wl = bi & 31;
+                const float pv = __shfl_sync(0xffffffffu, pr[0], wl);
+                const bool pop = lane == wl;
+#pragma unroll
+                for (int i = 0; i + 1 < NV; i++) {
+                    key[i] = pop ? key[i + 1] : key[i];
+                    ex[i] = pop ? ex[i + 1] : ex[i];
+                    pr[i] = pop ? pr[i + 1] : pr[i];
+                }
+                if (pop) {
+                    key[NV - 1] = 0u;
+                    ex[NV - 1] = INT_MAX;
+                }
+                if (lane == j) {
+                    my_val = pv;
+                    my_idx = bi;
+                }
+                sel_sum += pv;   // slot order, identical on every lane
+                kth = bv;
+            } else if (lane == 0 && gap_out) {
+                gap_out[tok] = kth - bv;
+            }
+        }
+    } else {
+    uint32_t taken = 0;
     for (int j = 0; j < rounds; j++) {
         float bv = -FLT_MAX;
         int bi = INT_MAX;
@@ -128,6 +188,7 @@ __device__ __forceinline__ void finish_token(float (&v)[NV], const float* __rest
         } else if (lane == 0 && gap_out) {
             gap_out[tok] = kth - bv;
         }
+    }
     }
     if (k >= E && lane == 0 && gap_out) gap_out[tok] = __int_as_float(0x7f800000);
     if (lane < k) {
@@ -202,6 +263,9 @@ router_gemv_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
 #pragma unroll
     for (int t = 0; t < kGemvTokensPerWarp; t++) live[t] = t0 + t < N;
     const int d8 = d & ~7;
+    // unrolled so that several chunks' loads of x are in flight at once (the loop is
+    // latency-bound otherwise: one x load per token per iteration)
+#pragma unroll 4
     for (int c = lane * 8; c < d8; c += 256) {
         float xv[kGemvTokensPerWarp][8];
 #pragma unroll

@@ -56,7 +56,8 @@ __global__ void split3_kernel(const float* __restrict__ W, int64_t n, __nv_bfloa
 
 __global__ void __launch_bounds__(RTHREADS, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                 int64_t N, int d, int E, float* __restrict__ logits, int32_t* err) {
+                 int64_t N, int d, int E, int slices_per_cta, float* __restrict__ logits,
+                 float* __restrict__ slice_out, int32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -75,7 +76,13 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const int m0 = blockIdx.x * RBM;
     const int e0 = blockIdx.y * REN;
     const int nk = (d + RBK - 1) / RBK;
-    const int nslices = (nk + SLICE_KB - 1) / SLICE_KB;
+    const int nslices_all = (nk + SLICE_KB - 1) / SLICE_KB;
+    // this CTA's slices of d: all of them, or (split over blockIdx.z) a contiguous run whose
+    // per-slice sums go to slice_out for router_slices_kernel to add in order
+    const int sl0 = blockIdx.z * slices_per_cta;
+    const int sl1 = min(nslices_all, sl0 + slices_per_cta);
+    const int nslices = sl1 > sl0 ? sl1 - sl0 : 0;
+    const int kb0 = sl0 * SLICE_KB, kb1 = min(nk, sl1 * SLICE_KB);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RSTAGES; s++) {
@@ -108,7 +115,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             int last_ph[RSTAGES];
             for (int i = 0; i < RSTAGES; i++) last_ph[i] = -1;
             bool ok = true;
-            for (int kb = 0; kb < nk; kb++) {
+            for (int kb = kb0; kb < kb1; kb++) {
                 if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
                     ok = false;
                     break;
@@ -147,8 +154,9 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-                const int kb_end = min(nk, (sl + 1) * SLICE_KB);
-                for (int kb = sl * SLICE_KB; kb < kb_end; kb++) {
+                const int kb_beg = kb0 + sl * SLICE_KB;
+                const int kb_end = min(kb1, kb_beg + SLICE_KB);
+                for (int kb = kb_beg; kb < kb_end; kb++) {
                     if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
                         ok = false;
                         break;
@@ -159,7 +167,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < RBK / 16; kk++)
                         umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                                  (kb > sl * SLICE_KB || kk > 0) ? 1u : 0u);
+                                  (kb > kb_beg || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);
                     if (++s == RSTAGES) {
                         s = 0;
@@ -197,6 +205,20 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&tempty[a]);
+            const int64_t tok = (int64_t)m0 + row;
+            const int ebase = e0 + wg * 32;
+            if (slice_out) {
+                // split over d: this slice's sum, for router_slices_kernel
+                if (tok < N) {
+                    float* dst = slice_out + ((int64_t)(sl0 + sl) * N + tok) * E + ebase;
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        if (ebase + j < E)
+                            dst[j] = (__uint_as_float(p2[j]) + __uint_as_float(p1[j])) +
+                                     __uint_as_float(p0[j]);
+                }
+                continue;
+            }
 #pragma unroll
             for (int j = 0; j < 32; j++) {
                 const float s = (__uint_as_float(p2[j]) + __uint_as_float(p1[j])) +
@@ -209,7 +231,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         }
         const int64_t tok = (int64_t)m0 + row;
         const int ebase = e0 + wg * 32;
-        if (ok && tok < N) {
+        if (ok && !slice_out && tok < N) {
             float* dst = logits + tok * E + ebase;
             if (ebase + 32 <= E && (E & 3) == 0) {
 #pragma unroll
@@ -232,7 +254,39 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     if (threadIdx.x == 0 && *abort_flag && err) atomicOr(err, MOE_DEVERR_TIMEOUT);
 }
 
+// Split over d: logits[t, e] = the compensated (Kahan) sum of the slice sums in slice order,
+// the same recurrence and order the unsplit kernel runs in its epilogue.
+__global__ void router_slices_kernel(const float* __restrict__ slice_out, int nslices, int64_t NE,
+                                     float* __restrict__ logits) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < NE;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = 0.f, cmp = 0.f;
+        for (int sl = 0; sl < nslices; sl++) {
+            const float y = slice_out[(int64_t)sl * NE + i] - cmp;
+            const float tt = acc + y;
+            cmp = (tt - acc) - y;
+            acc = tt;
+        }
+        logits[i] = acc;
+    }
+}
+
 }  // namespace
+
+int router_tc_split(int64_t N, int d, int E) {
+    const int64_t ctas = ((N + RBM - 1) / RBM) * ((E + REN - 1) / REN);
+    const int nslices = ((d + RBK - 1) / RBK + SLICE_KB - 1) / SLICE_KB;
+    if (N > 1024 || ctas * 2 > device_sm_count() || nslices < 2) return 1;
+    int64_t z = device_sm_count() / ctas;
+    if (z > nslices) z = nslices;
+    const int spc = (int)((nslices + z - 1) / z);
+    return (nslices + spc - 1) / spc;
+}
+
+size_t router_tc_logits_floats(int64_t N, int d, int E) {
+    const int nslices = ((d + RBK - 1) / RBK + SLICE_KB - 1) / SLICE_KB;
+    return (size_t)N * E * (router_tc_split(N, d, E) > 1 ? 1 + nslices : 1);
+}
 
 cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
                              __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s) {
@@ -248,8 +302,16 @@ cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const flo
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((N + RBM - 1) / RBM), (unsigned)((E + REN - 1) / REN));
-    router_tc_kernel<<<grid, RTHREADS, RSMEM, s>>>(mx, mw, N, d, E, logits, err);
+    const int nslices = ((d + RBK - 1) / RBK + SLICE_KB - 1) / SLICE_KB;
+    const int z = router_tc_split(N, d, E);
+    const int spc = (nslices + z - 1) / z;
+    float* slices = z > 1 ? logits + N * E : nullptr;   // the region is sized by router_tc_logits_floats
+    dim3 grid((unsigned)((N + RBM - 1) / RBM), (unsigned)((E + REN - 1) / REN), (unsigned)z);
+    router_tc_kernel<<<grid, RTHREADS, RSMEM, s>>>(mx, mw, N, d, E, spc, logits, slices, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || z == 1) return e;
+    const int64_t NE = N * E;
+    router_slices_kernel<<<(unsigned)((NE + 255) / 256), 256, 0, s>>>(slices, nslices, NE, logits);
     return cudaGetLastError();
 }
 
