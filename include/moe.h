@@ -185,6 +185,12 @@ MOE_API moe_status moe_combine(const moe_cfg *cfg, const void *y_perm, const int
  * moe_forward -- the whole layer: moe_route, moe_permute, moe_grouped_ffn, moe_combine on
  * one stream with no host synchronisation; intermediates live in the workspace (see
  * moe_forward_buffers).  Arguments as in the step calls; out [N,d] act dtype.
+ * For a bf16 batch of at most 128 tokens with shared experts, the shared experts run on a stream
+ * owned by the library, forked from `stream` when the call starts (after all work already on
+ * `stream`) and joined back before the combine: the call stays ordered on `stream`, including
+ * under stream capture.  Larger batches use `stream` only.  The same holds for
+ * moe_forward_traced and moe_forward_w4a16; there the "shared" phase then measures the wait
+ * for the join.
  */
 MOE_API moe_status moe_forward(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
                        const void *W_gate, const void *W_up, const void *W_down,

@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "bwd_internal.cuh"
 
 namespace moe {
@@ -207,9 +209,9 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     return MOE_OK;
 }
 
-moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
-                                 const void* x, const void* Wsg, const void* Wsu, const void* Wsd,
-                                 void* out, void* ws, cudaStream_t s, void* const* ev) {
+// The shared experts: Ysh = SwiGLU_s(x) for every token, into the workspace.
+moe_status do_shared(const moe_cfg* c, const void* x, const void* Wsg, const void* Wsu,
+                     const void* Wsd, void* ws, cudaStream_t s) {
     const WsLayout L = ws_layout(*c);
     int32_t* err = at<int32_t>(ws, L.err);
     void* hsh = at<void>(ws, L.h_sh);
@@ -246,9 +248,63 @@ moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int
                                    (float*)ysh, s));
         }
     }
+    return MOE_OK;
+}
+
+// Shared experts (unless already run on the side stream) and the combine, on s.
+moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
+                                 const void* x, const void* Wsg, const void* Wsu, const void* Wsd,
+                                 void* out, void* ws, cudaStream_t s, void* const* ev,
+                                 bool shared_done = false) {
+    const WsLayout L = ws_layout(*c);
+    if (!shared_done) MOE_TRY(do_shared(c, x, Wsg, Wsu, Wsd, ws, s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
-    MOE_CUDA(launch_combine(*c, y_perm, pos, ysh, out, err, s));
+    MOE_CUDA(launch_combine(*c, y_perm, pos, at<void>(ws, L.y_sh), out, at<int32_t>(ws, L.err), s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ side stream
+//
+// For a decode-sized batch the shared experts are a handful of tiles that would run alone with
+// most SMs idle; they depend only on x, so they are forked onto a library-owned stream at the
+// start of the forward and joined before the combine, overlapping the router, the permutation
+// and the routed experts.  Larger batches keep them in line (their GEMMs fill the GPU).
+constexpr int64_t kSideStreamMaxTokens = 128;
+
+bool fork_shared(const moe_cfg& c) {
+    return c.act_dtype == MOE_BF16 && c.n_shared > 0 && c.N > 0 && c.N <= kSideStreamMaxTokens;
+}
+
+cudaStream_t side_stream() {
+    static std::mutex mu;
+    static cudaStream_t streams[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+        streams[dev] = nullptr;
+    return streams[dev];
+}
+
+// Fork: the side stream waits for everything issued to s so far, then runs the shared experts;
+// *join is recorded after them.  The events are created per call (and destroyed by the caller
+// once s waits on join), so concurrent callers never share an event.
+moe_status fork_shared_begin(cudaStream_t s, cudaStream_t side, cudaEvent_t* join) {
+    cudaEvent_t fork = nullptr;
+    MOE_CUDA(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
+    cudaError_t e = cudaEventRecord(fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+    cudaEventDestroy(fork);
+    MOE_CUDA(e);
+    MOE_CUDA(cudaEventCreateWithFlags(join, cudaEventDisableTiming));
+    return MOE_OK;
+}
+moe_status fork_shared_end(cudaStream_t s, cudaStream_t side, cudaEvent_t join) {
+    cudaError_t e = cudaEventRecord(join, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, join, 0);
+    cudaEventDestroy(join);
+    MOE_CUDA(e);
     return MOE_OK;
 }
 
@@ -299,9 +355,8 @@ moe_status do_grouped_ffn_w4(const moe_cfg* c, const void* x_perm, const int32_t
     return MOE_OK;
 }
 
-moe_status do_shared_w4_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
-                                    const void* x, const moe_w4_layer& W, void* out, void* ws,
-                                    cudaStream_t s, void* const* ev) {
+moe_status do_shared_w4(const moe_cfg* c, const void* x, const moe_w4_layer& W, void* ws,
+                        cudaStream_t s) {
     const WsLayout L = ws_layout(*c);
     auto* hsh = at<__nv_bfloat16>(ws, L.h_sh);
     auto* ysh = at<__nv_bfloat16>(ws, L.y_sh);
@@ -315,8 +370,17 @@ moe_status do_shared_w4_and_combine(const moe_cfg* c, const void* y_perm, const 
         MOE_CUDA(w4_down(g, hsh, c->d_ff_shared, w4m(W.shared_down), c->d, nullptr, ysh,
                          at<int32_t>(ws, L.err), c->N * c->n_shared, s));
     }
+    return MOE_OK;
+}
+
+moe_status do_shared_w4_and_combine(const moe_cfg* c, const void* y_perm, const int32_t* pos,
+                                    const void* x, const moe_w4_layer& W, void* out, void* ws,
+                                    cudaStream_t s, void* const* ev, bool shared_done) {
+    const WsLayout L = ws_layout(*c);
+    if (!shared_done) MOE_TRY(do_shared_w4(c, x, W, ws, s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
-    MOE_CUDA(launch_combine(*c, y_perm, pos, ysh, out, at<int32_t>(ws, L.err), s));
+    MOE_CUDA(launch_combine(*c, y_perm, pos, at<__nv_bfloat16>(ws, L.y_sh), out,
+                            at<int32_t>(ws, L.err), s));
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
     return MOE_OK;
 }
@@ -477,6 +541,12 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
+    cudaEvent_t join = nullptr;
+    if (side) {
+        MOE_TRY(fork_shared_begin(s, side, &join));
+        MOE_TRY(do_shared(cfg, x, Ws_gate, Ws_up, Ws_down, ws, side));
+    }
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
@@ -493,8 +563,9 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     MOE_TRY(do_grouped_ffn(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                            at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), W_gate,
                            W_up, W_down, at<void>(ws, L.y_perm), ws, s, ev));
+    if (side) MOE_TRY(fork_shared_end(s, side, join));
     MOE_TRY(do_shared_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, Ws_gate,
-                                  Ws_up, Ws_down, out, ws, s, ev));
+                                  Ws_up, Ws_down, out, ws, s, ev, side != nullptr));
     return MOE_OK;
 }
 
@@ -554,6 +625,12 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
+    cudaEvent_t join = nullptr;
+    if (side) {
+        MOE_TRY(fork_shared_begin(s, side, &join));
+        MOE_TRY(do_shared_w4(cfg, x, *W, ws, side));
+    }
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
@@ -570,8 +647,9 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     MOE_TRY(do_grouped_ffn_w4(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                               at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), *W,
                               at<void>(ws, L.y_perm), ws, s, ev));
+    if (side) MOE_TRY(fork_shared_end(s, side, join));
     MOE_TRY(do_shared_w4_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, *W,
-                                     out, ws, s, ev));
+                                     out, ws, s, ev, side != nullptr));
     return MOE_OK;
 }
 
