@@ -66,12 +66,13 @@ __global__ void plan_shared_kernel(int S, int N, int Np, int32_t* rows, int32_t*
     }
 }
 
-// One warp per padded row: dout and x rows of routed groups (zeros in the padding).
+// One warp per padded row: dout and x rows of routed groups (zeros in the padding), both read
+// through the grouped row's token.
 __global__ void __launch_bounds__(256)
 gather_routed_kernel(const int32_t* __restrict__ c_off, const int32_t* __restrict__ kept,
                      const int32_t* __restrict__ kept_off, const int32_t* __restrict__ row_token,
                      int E, int64_t rows_bound, int d, const __nv_bfloat16* __restrict__ dout,
-                     const __nv_bfloat16* __restrict__ x_perm, __nv_bfloat16* __restrict__ dout_pad,
+                     const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ dout_pad,
                      __nv_bfloat16* __restrict__ x_pad) {
     const int64_t pr = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -81,7 +82,7 @@ gather_routed_kernel(const int32_t* __restrict__ c_off, const int32_t* __restric
     const bool valid = local < kept[g];
     const int64_t dr = kept_off[g] + local;
     const uint4* src_d = valid ? reinterpret_cast<const uint4*>(dout + (int64_t)row_token[dr] * d) : nullptr;
-    const uint4* src_x = valid ? reinterpret_cast<const uint4*>(x_perm + dr * d) : nullptr;
+    const uint4* src_x = valid ? reinterpret_cast<const uint4*>(x + (int64_t)row_token[dr] * d) : nullptr;
     uint4* dd = reinterpret_cast<uint4*>(dout_pad + pr * d);
     uint4* dx = reinterpret_cast<uint4*>(x_pad + pr * d);
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -422,7 +423,8 @@ cudaError_t run_backward(const BwdArgs& a, cudaStream_t s) {
     __nv_bfloat16* x_pad = at<__nv_bfloat16>(bw, L.x_pad);
     if (R > 0) {
         gather_routed_kernel<<<(unsigned)((Rp * 32 + 255) / 256), 256, 0, s>>>(
-            c_off, a.kept, a.kept_off, a.row_token, E, Rp, (int)d, a.dout, a.x_perm, dout_pad, x_pad);
+            c_off, a.kept, a.kept_off, a.row_token, E, Rp, (int)d, a.dout,
+            (const __nv_bfloat16*)a.x, dout_pad, x_pad);
     }
     __nv_bfloat16* dout_s = at<__nv_bfloat16>(bw, L.dout_s);
     __nv_bfloat16* x_s = at<__nv_bfloat16>(bw, L.x_s);

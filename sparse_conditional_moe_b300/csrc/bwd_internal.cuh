@@ -80,7 +80,7 @@ struct BwdArgs {
     int32_t *idx, *pos, *counts, *kept, *kept_off, *row_token, *err;
     float *w, *gap, *lse, *p_part, *P_sum, *row_weight, *logits;
     __nv_bfloat16* w3;
-    const __nv_bfloat16 *x_perm, *h_perm, *h_sh;
+    const __nv_bfloat16 *h_perm, *h_sh;
     void* bws;
 };
 cudaError_t run_backward(const BwdArgs& a, cudaStream_t s);

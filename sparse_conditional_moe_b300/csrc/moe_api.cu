@@ -738,7 +738,6 @@ moe_status moe_backward(const moe_cfg* cfg, const void* x, const float* W_r, con
     a.row_weight = at<float>(ws, L.row_weight);
     a.logits = at<float>(ws, L.logits);
     a.w3 = at<__nv_bfloat16>(ws, L.router_w3);
-    a.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
     a.h_perm = at<__nv_bfloat16>(ws, L.h_perm);
     a.h_sh = at<__nv_bfloat16>(ws, L.h_sh);
     a.bws = bws;

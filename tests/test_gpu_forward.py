@@ -105,6 +105,25 @@ def test_forward_is_deterministic_and_repeatable():
     assert torch.equal(out1, out2) and torch.equal(out2, out3)
 
 
+@pytest.mark.parametrize("spec", [s for s in SMALL if s.dtype == "bf16"], ids=lambda s: s.name)
+def test_forward_grouped_rows_match_the_step_path(spec):
+    """moe_forward's grouped outputs equal those of the step path fed with x_perm built here from
+    x and row_token (torch indexing): the same kernels in the same order, so bit-identical."""
+    dev = to_dev(moe_synth.make_layer(spec, seed=5))
+    lay, _ = run_layer(spec, dev)
+    b = lay.buffers()
+    cfg = moe.cfg_from_spec(spec)
+    R = moe.moe_grouped_rows(cfg)
+    M = int(b["kept_offsets"][spec.E].item())
+    x_perm = torch.zeros((max(R, 1), spec.d), dtype=torch.bfloat16, device="cuda")
+    x_perm[:M] = dev["x"][b["row_token"][:M].long()]
+    y = torch.full((max(R, 1), spec.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_ffn(cfg, x_perm, b["kept"], b["kept_offsets"], b["row_weight"],
+                        dev["W_gate"], dev["W_up"], dev["W_down"], y, lay.ws)
+    torch.cuda.synchronize()
+    assert M > 0 and torch.equal(y[:M], b["y_perm"][:M])
+
+
 def test_forward_empty_batch():
     spec = moe_synth.LayerSpec("empty", N=0, d=128, d_ff=128, E=8, k=2, n_shared=1,
                                d_ff_shared=128)
