@@ -423,6 +423,19 @@ class MoELayer:
                     stream, events)
         return out
 
+    def capture(self, x: torch.Tensor) -> "torch.cuda.CUDAGraph":
+        """Capture the forward on the static input buffer x into a CUDA graph (on a side stream,
+        as capture requires); each replay() recomputes self.out from x's current contents.  Run
+        one eager forward first so that the library's own streams exist before the capture."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g):
+                self.forward(x)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
     def buffers(self) -> dict:
         return moe_forward_buffers(self.cfg, self.ws)
 
