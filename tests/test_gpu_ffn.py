@@ -60,6 +60,16 @@ def test_grouped_ffn_bf16(d, F, rows):
     compare_rows(got, ref, spec, what="grouped ffn")
 
 
+def test_grouped_ffn_tail_tile_boundaries():
+    """Every boundary of the tail handling: a last m-tile of at most 96 rows is computed with the
+    operands swapped (N = its rows rounded up to 16, stored transposed through 32-row chunks),
+    97..127 rows as a masked 128-row tile; groups below, at and above 16, 32, 96, 128 rows."""
+    rows = [1, 15, 16, 17, 31, 32, 33, 95, 96, 97, 127, 128, 129, 144, 160, 223, 224, 225]
+    spec = moe_synth.LayerSpec("g", N=1, d=192, d_ff=320, E=len(rows), k=1)
+    got, ref = _grouped(spec, rows, seed=11)
+    compare_rows(got, ref, spec, what="grouped ffn tail tiles")
+
+
 @pytest.mark.parametrize("d,F,rows", [(128, 256, [16, 0, 65, 1]), (36, 20, [3, 70])])
 def test_grouped_ffn_fp32(d, F, rows):
     spec = moe_synth.LayerSpec("g", N=1, d=d, d_ff=F, E=len(rows), k=1, dtype="f32")
