@@ -279,8 +279,8 @@ def main():
     kept_rows, touched = st["kept_rows"], st["touched_experts"]
 
     # ---------------- device-timed region (inputs resident in HBM)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_TRACE_EVENTS)]
-          for _ in range(args.steps)]
+    # Plain forwards: the per-phase events below come from a separate traced pass, so that the
+    # seven event records per step do not add to the timed work of small, launch-bound layers.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_id_for_smi(torch, local))
     clocks.start()
@@ -289,7 +289,7 @@ def main():
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        lay.forward(xs[i % 2], events=ev[i])
+        lay.forward(xs[i % 2])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -298,10 +298,18 @@ def main():
     if lay.device_error() != 0:
         raise RuntimeError("device error during the timed region")
     ms_step = elapsed_ms / args.steps
+
+    # ---------------- per-phase breakdown (traced pass, not part of the timed region)
+    trace_steps = max(1, min(args.steps, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_TRACE_EVENTS)]
+          for _ in range(trace_steps)]
+    for i in range(trace_steps):
+        lay.forward(xs[i % 2], events=ev[i])
+    torch.cuda.synchronize()
     value = job_rate(spec.N, world, ms_step)
 
     phases = ["route", "permute", "gateup", "down", "shared", "combine"]
-    ph_ms = {p: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+    ph_ms = {p: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(trace_steps))
              for j, p in enumerate(phases)}
 
     # ---------------- roofline of the dominant kernel (routed gate/up grouped GEMM)
