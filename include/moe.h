@@ -203,7 +203,8 @@ MOE_API moe_status moe_forward(const moe_cfg *cfg, const void *x, const float *W
 /*
  * moe_forward_traced -- moe_forward that also records events[0..6] (cudaEvent_t as void*,
  * created by the caller) on stream: before routing and after routing, permutation,
- * routed gate/up GEMM, routed down GEMM, shared experts and combine.
+ * routed gate/up GEMM, routed down GEMM, shared experts and combine.  A NULL entry skips that
+ * record (e.g. only events[2] and events[3] to time the gate/up GEMM alone).
  */
 MOE_API moe_status moe_forward_traced(const moe_cfg *cfg, const void *x, const float *W_r,
                               const float *b_r, const void *W_gate, const void *W_up,

@@ -192,7 +192,7 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
         MOE_CUDA(simt_gateup_f32(g, (const float*)x_perm, c->d, (const float*)Wg,
                                  (const float*)Wu, c->d_ff, (float*)h, s));
     }
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
+    if (ev && ev[3]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
     if (pairs) {
         MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
                           row_weight, (__nv_bfloat16*)y_perm, err, s));
@@ -205,7 +205,7 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
         MOE_CUDA(simt_down_f32(g, (const float*)h, c->d_ff, (const float*)Wd, c->d, row_weight,
                                (float*)y_perm, s));
     }
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
+    if (ev && ev[4]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
     return MOE_OK;
 }
 
@@ -258,9 +258,9 @@ moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int
                                  bool shared_done = false) {
     const WsLayout L = ws_layout(*c);
     if (!shared_done) MOE_TRY(do_shared(c, x, Wsg, Wsu, Wsd, ws, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
+    if (ev && ev[5]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
     MOE_CUDA(launch_combine(*c, y_perm, pos, at<void>(ws, L.y_sh), out, at<int32_t>(ws, L.err), s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
+    if (ev && ev[6]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
     return MOE_OK;
 }
 
@@ -347,11 +347,11 @@ moe_status do_grouped_ffn_w4(const moe_cfg* c, const void* x_perm, const int32_t
     if (grouped_rows(*c) > 0)
         MOE_CUDA(w4_gateup(g, (const __nv_bfloat16*)x_perm, c->d, w4m(W.gate), w4m(W.up), c->d_ff,
                            h, at<int32_t>(ws, L.err), grouped_rows(*c), s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
+    if (ev && ev[3]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
     if (grouped_rows(*c) > 0)
         MOE_CUDA(w4_down(g, h, c->d_ff, w4m(W.down), c->d, row_weight, (__nv_bfloat16*)y_perm,
                          at<int32_t>(ws, L.err), grouped_rows(*c), s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
+    if (ev && ev[4]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[4], s));
     return MOE_OK;
 }
 
@@ -378,10 +378,10 @@ moe_status do_shared_w4_and_combine(const moe_cfg* c, const void* y_perm, const 
                                     cudaStream_t s, void* const* ev, bool shared_done) {
     const WsLayout L = ws_layout(*c);
     if (!shared_done) MOE_TRY(do_shared_w4(c, x, W, ws, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
+    if (ev && ev[5]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[5], s));
     MOE_CUDA(launch_combine(*c, y_perm, pos, at<__nv_bfloat16>(ws, L.y_sh), out,
                             at<int32_t>(ws, L.err), s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
+    if (ev && ev[6]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[6], s));
     return MOE_OK;
 }
 
@@ -540,7 +540,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     cudaStream_t s = (cudaStream_t)stream;
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    if (ev && ev[0]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
     cudaEvent_t join = nullptr;
     if (side) {
@@ -551,7 +551,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
+    if (ev && ev[1]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
                             at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                             at<int32_t>(ws, L.kept), at<int32_t>(ws, L.kept_offsets),
@@ -559,7 +559,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
                             at<int32_t>(ws, L.row_token), at<float>(ws, L.row_weight),
                             at<void>(ws, L.x_perm), at<int32_t>(ws, L.blk_hist),
                             at<int32_t>(ws, L.blk_base), err, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
+    if (ev && ev[2]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
     MOE_TRY(do_grouped_ffn(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                            at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), W_gate,
                            W_up, W_down, at<void>(ws, L.y_perm), ws, s, ev));
@@ -624,7 +624,7 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     cudaStream_t s = (cudaStream_t)stream;
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    if (ev && ev[0]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
     cudaEvent_t join = nullptr;
     if (side) {
@@ -635,7 +635,7 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
+    if (ev && ev[1]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
                             at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                             at<int32_t>(ws, L.kept), at<int32_t>(ws, L.kept_offsets),
@@ -643,7 +643,7 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
                             at<int32_t>(ws, L.row_token), at<float>(ws, L.row_weight),
                             at<void>(ws, L.x_perm), at<int32_t>(ws, L.blk_hist),
                             at<int32_t>(ws, L.blk_base), err, s));
-    if (ev) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
+    if (ev && ev[2]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[2], s));
     MOE_TRY(do_grouped_ffn_w4(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                               at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), *W,
                               at<void>(ws, L.y_perm), ws, s, ev));

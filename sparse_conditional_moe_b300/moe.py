@@ -274,12 +274,14 @@ def moe_grouped_ffn_w4a16(cfg, x_perm, kept, kept_offsets, row_weight, w4: dict,
 
 
 def _event_array(events, stream):
+    """MOE_TRACE_EVENTS torch events (None entries are not recorded) as a void* array."""
     if events is None:
         return None
     for e in events:                  # torch creates the CUDA event on its first record
-        if e.cuda_event == 0:
+        if e is not None and e.cuda_event == 0:
             e.record(stream if stream is not None else torch.cuda.current_stream())
-    return (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return (ctypes.c_void_p * MOE_TRACE_EVENTS)(
+        *[ctypes.c_void_p(e.cuda_event if e is not None else 0) for e in events])
 
 
 def moe_forward_w4a16(cfg, x, W_r, b_r, w4: dict, out, ws, stream=None, events=None):
