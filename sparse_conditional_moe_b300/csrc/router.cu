@@ -8,15 +8,17 @@
 // Three ways to get the logits, one epilogue:
 //   E <= 32      router_gemv_kernel: a warp per two tokens, lanes split d in 8-wide chunks,
 //                each lane accumulates E short fp32 chains, a butterfly shuffle sums them;
-//   E > 32, bf16 the tensor-core router of router_tc.cu writes fp32 logits [N, E], then
-//                logits_topk_kernel finishes each token;
+//   E > 32, bf16 the tensor-core router of router_tc.cu writes fp32 logits [N, E] (split
+//                over d for small N), then logits_topk_kernel finishes each token, one per
+//                warp;
 //   E > 32, fp32 router_tiled_kernel: BT tokens x all experts per block, DK-wide slices of x
 //                and W_r in shared memory, each slice an fp32 FMA chain, slices added to the
 //                running logit with compensated (Kahan) summation.
 // finish_token() is the common epilogue: each warp owns a token, lane l holds the logits of
 // experts l, l+32, ...; max and sum by warp shuffles; top-k by k rounds of a warp arg-max on
-// (probability desc, expert index asc); the (k+1)-th gives the near-tie gap; per-block column
-// sums of the probabilities go to p_part (deterministic, no float atomics).
+// (probability desc, expert index asc) -- each lane sorts its candidates once and offers its
+// head, two warp reductions pick the winner; the (k+1)-th gives the near-tie gap; per-block
+// column sums of the probabilities go to p_part (deterministic, no float atomics).
 #include <float.h>
 #include <limits.h>
 
