@@ -19,6 +19,9 @@
 //               single MMA-issuing thread (tcgen05.mma M=128, N=192, K=16);
 //   warps 2..9  two epilogue warpgroups, experts [0,32) and [32,64) of the tile.
 // Logits are written as fp32 [N, E]; softmax and top-k follow in router.cu.
+// Small batches (N <= 1024, few CTAs) split d over blockIdx.z: each CTA writes the sum of every
+// 256-wide slice it covers, and router_slices_kernel adds the slices in order with the same
+// Kahan recurrence, so the logits are bit-identical to the unsplit kernel's.
 #include "tc_ptx.cuh"
 
 namespace moe {
