@@ -208,17 +208,17 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_
 #pragma unroll
             for (int i = 0; i < 8; i++) a[i] = __ldg(src + v + 32 * i);
 #pragma unroll
-            for (int i = 0; i < 8; i++) dst[v + 32 * i] = a[i];
+            for (int i = 0; i < 8; i++) __stcs(dst + v + 32 * i, a[i]);   // streamed: read later by TMA
         }
         for (; v + 96 < row_vecs; v += 128) {   // four 16-byte loads in flight per lane
             const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
                         e = __ldg(src + v + 96);
-            dst[v] = a;
-            dst[v + 32] = b;
-            dst[v + 64] = c;
-            dst[v + 96] = e;
+            __stcs(dst + v, a);
+            __stcs(dst + v + 32, b);
+            __stcs(dst + v + 64, c);
+            __stcs(dst + v + 96, e);
         }
-        for (; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+        for (; v < row_vecs; v += 32) __stcs(dst + v, __ldg(src + v));
     }
 }
 
