@@ -6,9 +6,20 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "bwd_internal.cuh"
 
 namespace moe {
+
+// NVTX range over a host-side scope (an entry point or a phase of the forward), for timeline
+// tools; a no-op unless a profiler has injected its NVTX handler.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int device_sm_count() {
     static int cached[64] = {0};
@@ -442,6 +453,7 @@ moe_status moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, voi
 moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
                      int32_t* idx, float* w, float* P_sum, float* gap, void* ws, size_t ws_bytes,
                      void* stream) {
+    NvtxRange nvtx_("moe_route");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     if (cfg->N > 0) {
@@ -464,6 +476,7 @@ moe_status moe_permute(const moe_cfg* cfg, const int32_t* idx, const float* w, c
                        int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_offsets,
                        int32_t* perm, int32_t* pos, int32_t* row_token, float* row_weight,
                        void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_("moe_permute");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(need(counts, 4));
@@ -492,6 +505,7 @@ moe_status moe_grouped_ffn(const moe_cfg* cfg, const void* x_perm, const int32_t
                            const int32_t* kept_offsets, const float* row_weight,
                            const void* W_gate, const void* W_up, const void* W_down, void* y_perm,
                            void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_("moe_grouped_ffn");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(need(kept, 4));
@@ -509,6 +523,7 @@ moe_status moe_grouped_ffn(const moe_cfg* cfg, const void* x_perm, const int32_t
 moe_status moe_combine(const moe_cfg* cfg, const void* y_perm, const int32_t* pos, const void* x,
                        const void* Ws_gate, const void* Ws_up, const void* Ws_down, void* out,
                        void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_("moe_combine");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(check_shared(cfg, Ws_gate, Ws_up, Ws_down));
@@ -527,6 +542,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
                               const void* W_down, const void* Ws_gate, const void* Ws_up,
                               const void* Ws_down, void* out, void* ws, size_t ws_bytes,
                               void* stream, void* const* ev) {
+    NvtxRange nvtx_("moe_forward_traced");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(need(W_r, 16));
@@ -593,6 +609,7 @@ moe_status moe_grouped_ffn_w4a16(const moe_cfg* cfg, const void* x_perm, const i
                                  const int32_t* kept_offsets, const float* row_weight,
                                  const moe_w4_layer* W, void* y_perm, void* ws, size_t ws_bytes,
                                  void* stream) {
+    NvtxRange nvtx_("moe_grouped_ffn_w4a16");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_w4_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
@@ -611,6 +628,7 @@ moe_status moe_grouped_ffn_w4a16(const moe_cfg* cfg, const void* x_perm, const i
 moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r, const float* b_r,
                              const moe_w4_layer* W, void* out, void* ws, size_t ws_bytes,
                              void* stream, void* const* ev) {
+    NvtxRange nvtx_("moe_forward_w4a16");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_w4_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
@@ -675,6 +693,7 @@ moe_status moe_backward(const moe_cfg* cfg, const void* x, const float* W_r, con
                         float* db, float* dW_gate, float* dW_up, float* dW_down, float* dWs_gate,
                         float* dWs_up, float* dWs_down, void* ws, size_t ws_bytes, void* bws,
                         size_t bws_bytes, void* stream) {
+    NvtxRange nvtx_("moe_backward");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_bwd_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
@@ -772,6 +791,7 @@ moe_status moe_router_stats(const moe_cfg* cfg, const float* lse, const float* w
                             const int32_t* perm, const int32_t* offsets, float* importance_host,
                             moe_router_summary* summary, void* ws, size_t ws_bytes,
                             void* stream) {
+    NvtxRange nvtx_("moe_router_stats");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     if (!summary) return MOE_ERR_INVALID_ARG;
@@ -818,6 +838,7 @@ moe_status moe_stats(const moe_cfg* cfg, const int32_t* counts, const int32_t* k
                      const float* P_sum, const int32_t* pos, const float* gap, float* f_host,
                      float* P_host, moe_stats_summary* summary, void* ws, size_t ws_bytes,
                      void* stream) {
+    NvtxRange nvtx_("moe_stats");
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     MOE_TRY(need(counts, 4));
