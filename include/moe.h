@@ -393,6 +393,8 @@ MOE_API moe_status moe_selftest_gemm(int32_t a_mn, int32_t b_mn, int32_t M, int3
 MOE_API moe_status moe_device_error(void *ws, size_t ws_bytes, int32_t *code_host, void *stream);
 
 MOE_API const char *moe_status_string(moe_status s);
+/* The same string under the short name. */
+MOE_API const char *moe_status_str(moe_status s);
 
 #ifdef __cplusplus
 }

@@ -431,6 +431,8 @@ const char* moe_status_string(moe_status s) {
     return "unknown status";
 }
 
+const char* moe_status_str(moe_status s) { return moe_status_string(s); }
+
 int64_t moe_grouped_rows(const moe_cfg* cfg) {
     if (check_cfg(cfg) != MOE_OK) return -1;
     return grouped_rows(*cfg);

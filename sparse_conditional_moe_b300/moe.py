@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_route",
            "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
-           "moe_selftest_wait_timeout", "moe_status_string", "moe_quantize_w4",
+           "moe_selftest_wait_timeout", "moe_status_string", "moe_status_str", "moe_quantize_w4",
            "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats",
            "moe_selftest_gemm", "moe_backward_workspace_size", "moe_backward")
 MOE_W4_GROUP = 128
