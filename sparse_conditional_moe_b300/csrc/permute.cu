@@ -10,7 +10,8 @@
 // The stable sort is rebuilt from integer counting, so it is bit-identical to a stable
 // argsort and does not depend on thread timing:
 //   count   : block b counts its 2048 consecutive slots per expert (per-warp rows in
-//             shared memory, warp-aggregated with __match_any_sync) -> blk_hist[b][e]
+//             shared memory, warp-aggregated with __match_any_sync; the block's slots split
+//             evenly over its warps, in order) -> blk_hist[b][e]
 //   scan    : one block turns blk_hist into counts, offsets (exclusive scan over e),
 //             kept = min(counts, C), kept_offsets, and blk_base[b][e] = offsets-free
 //             prefix of blk_hist over blocks b' < b
@@ -30,11 +31,23 @@ __device__ __forceinline__ void set_err(int32_t* err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
-// Per-warp expert counts of this block's slots into cnt[warp][e] (E entries per warp).
+// This warp's slots: the block's slots (kPermSlotsPerBlock, fewer in the last block) in equal
+// consecutive runs of a multiple of 32, warp after warp, so a small last block (a decode batch
+// has a few hundred slots) still spreads over all warps.  Returns the run length; *f0 its start.
+__device__ __forceinline__ int warp_slots(int64_t A, int64_t* f0) {
+    const int64_t b0 = (int64_t)blockIdx.x * kPermSlotsPerBlock;
+    const int64_t left = A - b0;
+    const int64_t in_block = left < kPermSlotsPerBlock ? left : kPermSlotsPerBlock;
+    const int spw = (int)(((in_block + kWarps - 1) / kWarps + 31) / 32 * 32);
+    *f0 = b0 + (int64_t)(threadIdx.x / 32) * spw;
+    return spw;
+}
+
+// Per-warp expert counts of the warp's slots into cnt[warp][e] (E entries per warp).
 __device__ __forceinline__ void warp_count(const int32_t* __restrict__ idx, int64_t A, int E,
-                                           int64_t f_begin, int* cnt_row, int32_t* err) {
+                                           int64_t f_begin, int spw, int* cnt_row, int32_t* err) {
     const int lane = threadIdx.x & 31;
-    for (int step = 0; step < kPermSlotsPerWarp / 32; step++) {
+    for (int step = 0; step < spw / 32; step++) {
         int64_t f = f_begin + step * 32 + lane;
         int e = -1;
         if (f < A) {
@@ -58,8 +71,9 @@ perm_count_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __
     const int warp = threadIdx.x / 32;
     for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
-    int64_t f0 = (int64_t)blockIdx.x * kPermSlotsPerBlock + (int64_t)warp * kPermSlotsPerWarp;
-    warp_count(idx, A, E, f0, cnt + warp * E, err);
+    int64_t f0 = 0;
+    const int spw = warp_slots(A, &f0);
+    warp_count(idx, A, E, f0, spw, cnt + warp * E, err);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kPermThreads) {
         int s = 0;
@@ -139,8 +153,9 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
-    const int64_t f0 = (int64_t)blockIdx.x * kPermSlotsPerBlock + (int64_t)warp * kPermSlotsPerWarp;
-    warp_count(idx, A, E, f0, cnt + warp * E, nullptr);
+    int64_t f0 = 0;
+    const int spw = warp_slots(A, &f0);
+    warp_count(idx, A, E, f0, spw, cnt + warp * E, nullptr);
     __syncthreads();
     // per expert: exclusive scan over warps, starting at this block's base
     for (int e = threadIdx.x; e < E; e += kPermThreads) {
@@ -154,7 +169,7 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w
     __syncthreads();
     int* base = cnt + warp * E;
     const unsigned lt = (1u << lane) - 1u;
-    for (int step = 0; step < kPermSlotsPerWarp / 32; step++) {
+    for (int step = 0; step < spw / 32; step++) {
         int64_t f = f0 + step * 32 + lane;
         int e = -1;
         if (f < A) {
