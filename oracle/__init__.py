@@ -10,6 +10,7 @@ follows in the C source.  Parity pins for each function are in
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 from typing import Optional, Sequence
@@ -34,14 +35,28 @@ class W4Mat(ctypes.Structure):
 
 
 def build(force: bool = False) -> str:
-    """Compile moe_oracle.c into liboracle.so with gcc (OpenMP over tokens)."""
+    """Compile moe_oracle.c into liboracle.so with gcc (OpenMP over tokens).  Rebuilt when the
+    SHA-256 of the source and the compile line differs from the one stored beside the library."""
     if _OVERRIDE:
         return _OVERRIDE
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"]
+    h = hashlib.sha256(" ".join(cmd).encode())
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    key = h.hexdigest()
+    key_path = _LIB_PATH + ".key"
+    try:
+        with open(key_path) as f:
+            stored = f.read().strip()
+    except OSError:
+        stored = ""
+    if force or not os.path.exists(_LIB_PATH) or stored != key:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        subprocess.check_call(cmd + ["-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
+        with open(key_path + f".tmp{os.getpid()}", "w") as f:
+            f.write(key + "\n")
+        os.replace(key_path + f".tmp{os.getpid()}", key_path)
     return _LIB_PATH
 
 
