@@ -149,62 +149,6 @@ plan_kernel(const int32_t* __restrict__ kept, int E, int bm, int32_t* __restrict
     if (e == 0) mtile_off[E] = tmp[32];
 }
 
-// Inclusive warp scan then block-wide exclusive scan of one int per thread (1024 threads).
-__device__ __forceinline__ int block_excl_scan(int v, int* tmp /*[33]*/, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-    }
-    if (lane == 31) tmp[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        const int wv = tmp[lane];
-        int winc = wv;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, winc, off);
-            if (lane >= off) winc += o;
-        }
-        tmp[lane] = winc - wv;
-        if (lane == 31) tmp[32] = winc;
-    }
-    __syncthreads();
-    const int r = tmp[warp] + inc - v;
-    *total = tmp[32];
-    __syncthreads();
-    return r;
-}
-
-// Split every group of rows into full 256-row pairs (CTA-pair kernel) and at most one 128-row
-// tail m-tile (single-CTA kernel): with mt = ceil(kept/128), the group has mt/2 pairs and, when
-// mt is odd, a tail of kept - (mt-1)*128 rows starting at row (mt-1)*128 of the group.
-__global__ void __launch_bounds__(1024)
-plan_pairs_kernel(const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_off, int E,
-                  int32_t* __restrict__ pair_off, int32_t* __restrict__ tail_mtile,
-                  int32_t* __restrict__ tail_rows, int32_t* __restrict__ tail_off) {
-    __shared__ int tmp[33];
-    const int e = threadIdx.x;
-    const int rows = e < E ? kept[e] : 0;
-    const int mt = (rows + 127) / 128;
-    const int tail = mt & 1;
-    int tot_pairs, tot_tails;
-    const int pairs_before = block_excl_scan(mt >> 1, tmp, &tot_pairs);
-    const int tails_before = block_excl_scan(tail, tmp, &tot_tails);
-    if (e < E) {
-        pair_off[e] = pairs_before;
-        tail_mtile[e] = tails_before;
-        tail_rows[e] = tail ? rows - (mt - 1) * 128 : 0;
-        tail_off[e] = kept_off[e] + (tail ? (mt - 1) * 128 : 0);
-    }
-    if (e == 0) {
-        pair_off[E] = tot_pairs;
-        tail_mtile[E] = tot_tails;
-    }
-}
-
 // counters[0] fully dropped tokens, [1] near-tie tokens (counters zeroed by the caller)
 __global__ void stats_tokens_kernel(const int32_t* __restrict__ pos, const float* __restrict__ gap,
                                     int64_t N, int k, int32_t* counters) {
@@ -341,13 +285,6 @@ cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* 
 cudaError_t launch_plan_mtiles(const int32_t* kept, int E, int bm, int32_t* mtile_off,
                                cudaStream_t s) {
     plan_kernel<<<1, 1024, 0, s>>>(kept, E, bm, mtile_off);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_plan_pairs(const int32_t* kept, const int32_t* kept_off, int E,
-                              int32_t* pair_off, int32_t* tail_mtile, int32_t* tail_rows,
-                              int32_t* tail_off, cudaStream_t s) {
-    plan_pairs_kernel<<<1, 1024, 0, s>>>(kept, kept_off, E, pair_off, tail_mtile, tail_rows, tail_off);
     return cudaGetLastError();
 }
 

@@ -34,17 +34,16 @@ int device_sm_count() {
     return cached[dev];
 }
 
-// CTA pairs (cta_group::2) are opt-in with MOE_TC_PAIRS=1, for groups averaging >= 512 rows.
-// Measured on B300: 1577 vs 1473 TFLOP/s on eight equal 1024-row groups, but on routed layers,
-// whose group sizes straddle multiples of 256, the single-CTA kernel is as fast or faster, so it
-// is the default.
-bool use_cta_pairs(int64_t avg_rows) {
+// The bf16 forward's grouped GEMMs run on the CTA-pair kernels of grouped_gemm_pair.cu;
+// MOE_GROUPED_GEMM=single (read once per process) selects the single-CTA kernels of
+// grouped_gemm_tc.cu instead, for comparisons.
+bool use_pair_gemm() {
     static int enabled = -1;
     if (enabled < 0) {
-        const char* e = getenv("MOE_TC_PAIRS");
-        enabled = (e && atoi(e) != 0) ? 1 : 0;
+        const char* e = getenv("MOE_GROUPED_GEMM");
+        enabled = (e && strcmp(e, "single") == 0) ? 0 : 1;
     }
-    return enabled == 1 && avg_rows >= 512;
+    return enabled == 1;
 }
 
 int64_t capacity(const moe_cfg& c) {
@@ -81,7 +80,6 @@ WsLayout ws_layout(const moe_cfg& c) {
     L.blk_hist = take(4 * (size_t)perm_blocks(A) * E);
     L.blk_base = take(4 * (size_t)perm_blocks(A) * E);
     L.mtile_off = take(4 * (size_t)(E + 1));
-    L.tail_plan = take(4 * (size_t)(3 * E + 1));
     L.stats_f = take(4 * (size_t)(2 * E + 8));
     L.idx = take(4 * (size_t)A);
     L.w = take(4 * (size_t)A);
@@ -170,32 +168,23 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     int32_t* mtile = at<int32_t>(ws, L.mtile_off);
     const int64_t R = grouped_rows(*c);
     const bool bf16 = c->act_dtype == MOE_BF16;
-    const bool pairs = bf16 && use_cta_pairs(R / c->E);
+    const bool pair_gemm = bf16 && use_pair_gemm();
+    // no group holds more rows than tokens (top-k picks distinct experts) or than the capacity
+    const int64_t cap = capacity(*c);
+    const int64_t max_group_rows = cap >= 0 && cap < c->N ? cap : c->N;
     GroupGeom g{};
     g.G = c->E;
     g.rows = kept;
     g.row_off = kept_offsets;
     g.mtile_off = mtile;
     g.max_rows = R;
-    GroupGeom tail{};   // pair mode: the odd 128-row m-tile of each group, on the single-CTA kernel
-    if (pairs) {
-        int32_t* tp = at<int32_t>(ws, L.tail_plan);
-        MOE_CUDA(launch_plan_pairs(kept, kept_offsets, c->E, mtile, tp, tp + c->E + 1,
-                                   tp + 2 * c->E + 1, s));
-        tail.G = c->E;
-        tail.mtile_off = tp;
-        tail.rows = tp + c->E + 1;
-        tail.row_off = tp + 2 * c->E + 1;
-        tail.max_rows = (int64_t)c->E * kTcBlockRows;
-    } else {
-        MOE_CUDA(launch_plan_mtiles(kept, c->E, bf16 ? kTcBlockRows : simt_block_rows(), mtile, s));
-    }
+    const int bm = pair_gemm ? pair_chunk_rows() : bf16 ? kTcBlockRows : simt_block_rows();
+    MOE_CUDA(launch_plan_mtiles(kept, c->E, bm, mtile, s));
     void* h = at<void>(ws, L.h_perm);
-    if (pairs) {
-        MOE_CUDA(tc2_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
-                            (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, err, s));
-        MOE_CUDA(tc_gateup(tail, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
-                           (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
+    if (pair_gemm) {
+        MOE_CUDA(pair_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
+                             (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err,
+                             max_group_rows, s));
     } else if (bf16) {
         MOE_CUDA(tc_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
                            (const __nv_bfloat16*)Wu, c->d_ff, (__nv_bfloat16*)h, R, err, s));
@@ -204,11 +193,9 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
                                  (const float*)Wu, c->d_ff, (float*)h, s));
     }
     if (ev && ev[3]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[3], s));
-    if (pairs) {
-        MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
-                          row_weight, (__nv_bfloat16*)y_perm, err, s));
-        MOE_CUDA(tc_down(tail, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
-                         row_weight, (__nv_bfloat16*)y_perm, R, err, s));
+    if (pair_gemm) {
+        MOE_CUDA(pair_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
+                           row_weight, (__nv_bfloat16*)y_perm, R, err, max_group_rows, s));
     } else if (bf16) {
         MOE_CUDA(tc_down(g, (const __nv_bfloat16*)h, R, c->d_ff, (const __nv_bfloat16*)Wd, c->d,
                          row_weight, (__nv_bfloat16*)y_perm, R, err, s));
@@ -233,14 +220,15 @@ moe_status do_shared(const moe_cfg* c, const void* x, const void* Wsg, const voi
         g.G = S;
         g.uniform_rows = (int)c->N;
         g.max_rows = c->N;
-        if (c->act_dtype == MOE_BF16 && use_cta_pairs(c->N)) {
+        if (c->act_dtype == MOE_BF16 && use_pair_gemm()) {
             g.a_stride = 0;        // every shared expert reads all tokens of x
             g.c_stride = c->N;
-            MOE_CUDA(tc2_gateup(g, (const __nv_bfloat16*)x, c->N, c->d, (const __nv_bfloat16*)Wsg,
-                                (const __nv_bfloat16*)Wsu, Fs, (__nv_bfloat16*)hsh, err, s));
+            MOE_CUDA(pair_gateup(g, (const __nv_bfloat16*)x, c->N, c->d, (const __nv_bfloat16*)Wsg,
+                                 (const __nv_bfloat16*)Wsu, Fs, (__nv_bfloat16*)hsh, S * c->N, err,
+                                 c->N, s));
             g.a_stride = c->N;
-            MOE_CUDA(tc2_down(g, (const __nv_bfloat16*)hsh, S * c->N, Fs, (const __nv_bfloat16*)Wsd,
-                              c->d, nullptr, (__nv_bfloat16*)ysh, err, s));
+            MOE_CUDA(pair_down(g, (const __nv_bfloat16*)hsh, S * c->N, Fs, (const __nv_bfloat16*)Wsd,
+                               c->d, nullptr, (__nv_bfloat16*)ysh, S * c->N, err, c->N, s));
         } else if (c->act_dtype == MOE_BF16) {
             g.a_stride = 0;        // every shared expert reads all tokens of x
             g.c_stride = c->N;

@@ -33,8 +33,7 @@ struct WsLayout {
     size_t logits;       // float [N, E] (tensor-core router)
     size_t blk_hist;     // int32 [perm_blocks * E]
     size_t blk_base;     // int32 [perm_blocks * E]
-    size_t mtile_off;    // int32 [E + 1]: m-tile (or m-pair) prefix of the routed grouped GEMMs
-    size_t tail_plan;    // int32 [3E + 1]: tail m-tile prefix, tail rows, tail row offsets
+    size_t mtile_off;    // int32 [E + 1]: m-tile (or token-chunk) prefix of the routed grouped GEMMs
     size_t stats_f;      // float [2E + 8]: f, P, scalars
     size_t idx, w, gap, lse, P_sum, counts, offsets, kept, kept_offsets, perm, pos;
     size_t rstat;        // double [kRouterStatBlocks + E]: z-loss partials, importance
@@ -98,21 +97,21 @@ cudaError_t tc_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, 
                     const __nv_bfloat16* Wd, int D, const float* row_scale,
                     __nv_bfloat16* Y, int64_t y_rows, int32_t* err, cudaStream_t s);
 
-// The same two GEMMs on CTA pairs (tcgen05 cta_group::2, 256-row m-pairs; GroupGeom.mtile_off
-// then holds m-pair offsets).
-cudaError_t tc2_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
-                       const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
-                       __nv_bfloat16* H, int32_t* err, cudaStream_t s);
-cudaError_t tc2_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
-                     const __nv_bfloat16* Wd, int D, const float* row_scale, __nv_bfloat16* Y,
-                     int32_t* err, cudaStream_t s);
-// Whether groups of about `avg_rows` rows run on CTA pairs (see moe_api.cu).
-bool use_cta_pairs(int64_t avg_rows);
-// Pair/tail split of the routed groups: pair_off [E+1] prefix of full 256-row pairs;
-// tail_mtile [E+1] prefix of tail m-tiles (0 or 1 per group); tail_rows/tail_off [E].
-cudaError_t launch_plan_pairs(const int32_t* kept, const int32_t* kept_off, int E,
-                              int32_t* pair_off, int32_t* tail_mtile, int32_t* tail_rows,
-                              int32_t* tail_off, cudaStream_t s);
+// The grouped GEMMs on CTA pairs with the weights as the MMA's M side (grouped_gemm_pair.cu):
+// groups are cut into chunks of at most pair_chunk_rows() token rows (GroupGeom.mtile_off then
+// holds the chunk prefix); max_group_rows bounds any group's rows (it picks the decode-sized
+// variant when <= 64).
+int pair_chunk_rows();
+cudaError_t pair_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
+                        const __nv_bfloat16* Wg, const __nv_bfloat16* Wu, int F,
+                        __nv_bfloat16* H, int64_t h_rows, int32_t* err, int64_t max_group_rows,
+                        cudaStream_t s);
+cudaError_t pair_down(const GroupGeom& g, const __nv_bfloat16* H, int64_t h_rows, int F,
+                      const __nv_bfloat16* Wd, int D, const float* row_scale,
+                      __nv_bfloat16* Y, int64_t y_rows, int32_t* err, int64_t max_group_rows,
+                      cudaStream_t s);
+// Which bf16 grouped GEMM engine the forward uses: the pair kernels unless MOE_GROUPED_GEMM=single.
+bool use_pair_gemm();
 
 // fp32 CUDA-core grouped GEMMs (fp32 layers); their m-tiles are simt_block_rows() tall
 int simt_block_rows();
