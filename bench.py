@@ -3,20 +3,24 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one moe_forward (router, permute, grouped gate/up and down GEMMs, shared experts,
-combine) over one resident batch of the named workload; the default workload is the
-Mixtral-shaped bf16 layer (N=4096, d=4096, d_ff=14336, E=8, top-2).  Weights (2.8 GB) exceed the
-126 MB L2, so no flush is needed between steps.  `value` is tokens/s over all ranks from CUDA
-events; `e2e` repeats the measurement through the same C ABI with every step's batch copied in
-from pinned host memory and its output copied back (the copies on their own streams, double
-buffered, overlapping the neighbouring steps' layers).  `roofline` reports the dominant kernel (the
-routed gate/up grouped GEMM) against the measured bf16 peak.  `cpu_baseline` times the CPU oracle
-on a bounded sub-batch of the same layer.  Under torchrun (N > 1) every rank runs its own replica
-(the layer needs no exchange between GPUs).  The W4A16 workload runs moe_forward_w4a16 on expert
-weights quantised once by the library before timing.
+combine) over one resident batch of the named workload.  The default workload, and the headline
+`value`, is the DeepSeek-V3-shaped prefill layer (N=8192, d=7168, d_ff=2048, E=256, top-8, one
+shared expert): the largest layer of the workload set that fits one GPU.  Its weights (22.5 GB)
+exceed the 126 MB L2, so no flush is needed between steps.  `value` is tokens/s over all ranks
+from CUDA events around the K timed steps; `e2e` repeats the measurement through the same C ABI
+with every step's batch copied in from pinned host memory and its output copied back;
+`roofline` reports the dominant kernel (the routed gate/up grouped GEMM) against the measured
+burst bf16 peak; `workloads` repeats the device-timed measurement, with the same K and W, on
+the other layers of the set (Mixtral-shaped, DeepSeek-V3-shaped decode with bf16 and with
+W4A16 expert weights, Qwen3-30B-A3B-shaped skewed); `cpu_baseline` times the CPU oracle on a
+bounded sample of the headline layer.  Under torchrun (N > 1) every rank runs its own replica
+(the layer needs no exchange between GPUs).
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import os
 import statistics
@@ -34,96 +38,147 @@ import moe_synth  # noqa: E402
 from sparse_conditional_moe_b300 import accounting  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+HEADLINE = moe_synth.DSV3_PREFILL
+SIDE_WORKLOADS = (moe_synth.MIXTRAL, moe_synth.DSV3_DECODE, moe_synth.DSV3_DECODE_W4,
+                  moe_synth.QWEN3_SKEWED)
+# the library forks the shared experts of bf16 batches of at most this many tokens onto its
+# side stream, so the per-phase events on the caller's stream do not bracket them
+SIDE_STREAM_MAX_TOKENS = 128
 
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        d = json.load(open(p))
-        return d, "measured"
+        return json.load(open(p)), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
 
 
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clocks and throttle reasons sampled every few milliseconds during a timed region,
+    through NVML (nvidia-smi polling as a fallback)."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.lines = []
-        self.thread = None
+    def __init__(self, uuid: str, period_s: float = 0.004):
+        self.uuid = uuid
+        self.period = period_s
+        self.samples = []      # (sm_mhz, max_mhz, power_w, reasons bitmask)
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._proc = None
 
     def start(self):
+        self.nvml_error = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
-            self.proc = None
+            import pynvml
+            pynvml.nvmlInit()
+            try:
+                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
+            except Exception:   # noqa: BLE001 -- older bindings want bytes
+                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid.encode())
+            self._nvml = (pynvml, h)
+            self._max = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:   # noqa: BLE001 -- fall back to nvidia-smi polling
+            self.nvml_error = f"{type(e).__name__}: {e}"
+            self._nvml = None
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
-    def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
         try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+            fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.uuid}", f"--query-gpu={fields}",
+                 "--format=csv,noheader,nounits", "-lms", "10"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thread = threading.Thread(target=self._read_smi, daemon=True)
+            self._thread.start()
+        except (OSError, ValueError):
+            self._proc = None
+
+    def _reasons(self, h):
+        pynvml = self._nvml[0]
+        f = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        return f(h)
+
+    def _poll(self):
+        pynvml, h = self._nvml
+        while not self._stop.is_set():
+            try:
+                sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                pw = pynvml.nvmlDeviceGetPowerUsage(h) / 1000.0
+                rs = self._reasons(h)
+                self.samples.append((float(sm), float(self._max), pw, int(rs)))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def _read_smi(self):
+        for ln in self._proc.stdout:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 7:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                bits = sum(b for (_, b), v in zip(self.REASONS, parts[3:7]) if v.lower() == "active")
+                self.samples.append((float(parts[0]), float(parts[1]), float(parts[2]), bits))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+
+    def stop(self) -> dict:
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self._nvml is not None:
+            try:
+                self._nvml[0].nvmlShutdown()
+            except Exception:
+                pass
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no clock samples (NVML and nvidia-smi unavailable)"]}
+        reasons = sorted({n for n, b in self.REASONS for s in self.samples if s[3] & b})
+        out = {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_min_mhz": min(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples),
+                "power_w_max": max(s[2] for s in self.samples),
+                "samples": len(self.samples),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi",
+                "reasons": reasons}
+        if self.nvml_error:
+            out["nvml_error"] = self.nvml_error
+        return out
 
 
-def gpu_id_for_smi(torch, local: int) -> str:
-    """nvidia-smi --id of the device torch uses (its UUID, so CUDA_VISIBLE_DEVICES is honoured)."""
-    try:
-        u = str(torch.cuda.get_device_properties(local).uuid)
-        return u if u.startswith("GPU-") else "GPU-" + u
-    except Exception:
-        return str(local)
+def gpu_uuid(torch, local: int) -> str:
+    """The NVML/nvidia-smi id of the device torch uses (its UUID, so CUDA_VISIBLE_DEVICES is
+    honoured)."""
+    u = str(torch.cuda.get_device_properties(local).uuid)
+    return u if u.startswith("GPU-") else "GPU-" + u
 
 
 # ------------------------------------------------------------------ CPU oracle leg
 
-def cpu_oracle_rate(spec, layer_host: dict, budget_s: float, max_steps: int = 0):
-    """Oracle forward over consecutive sub-batches of the layer until budget_s elapses.
-    Returns (tokens/s, tokens processed, seconds, sub-batch size, cores)."""
+def cpu_oracle_rate(spec, layer_host: dict, budget_s: float, max_steps: int = 0, sub: int = 0):
+    """Oracle forward over consecutive sub-batches of the layer until budget_s elapses (each
+    sub-batch is routed as a batch of its own).  Returns (tokens/s, tokens, seconds, sub-batch
+    size, cores)."""
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0))
     code = oracle.BF16 if spec.dtype == "bf16" else oracle.F32
-    sub = max(1, min(spec.N, cores))
+    sub = sub or max(1, min(spec.N, cores))
     x = layer_host["x"]
     done, t_used, steps = 0, 0.0, 0
     start = 0
@@ -142,6 +197,25 @@ def cpu_oracle_rate(spec, layer_host: dict, budget_s: float, max_steps: int = 0)
         if t_used >= budget_s or (max_steps and steps >= max_steps):
             break
     return done / t_used, done, t_used, sub, cores
+
+
+def cpu_oracle_one_core(spec, layer_host: dict, tokens: int = 2):
+    """The oracle on one thread over `tokens` tokens (OpenMP restricted to one thread for the
+    call), extrapolated linearly to tokens/s of one core."""
+    import oracle
+    try:
+        gomp = ctypes.CDLL("libgomp.so.1")
+        prev = gomp.omp_get_max_threads()
+        gomp.omp_set_num_threads(1)
+    except OSError:
+        return None
+    try:
+        rate, done, secs, sub, _ = cpu_oracle_rate(spec, layer_host, 0.0, max_steps=1, sub=tokens)
+    finally:
+        gomp.omp_set_num_threads(prev)
+    return {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} tokens of {spec.name} on one thread ({secs:.1f} s), extrapolated "
+                      f"linearly to tokens/s"}
 
 
 _W4_ORACLE_WEIGHTS = {}
@@ -179,6 +253,14 @@ def _oracle_w4_batch(spec, L) -> float:
     return t_route + time.perf_counter() - t0
 
 
+def cpu_sample_note(spec, sub: int) -> str:
+    note = f"consecutive sub-batches of {sub} tokens, each routed as its own batch"
+    if spec.capacity_factor > 0:
+        c = int(np.ceil(spec.capacity_factor * sub * spec.k / spec.E))
+        note += f" (so with its own capacity C = {c}, not the full batch's)"
+    return note
+
+
 # ------------------------------------------------------------------ several ranks (replicas)
 
 def max_over_ranks(ms: float, world: int, device) -> float:
@@ -199,64 +281,71 @@ def job_rate(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
 
 
 def metric_name(spec) -> str:
-    if spec == moe_synth.MIXTRAL:
-        return "MoE layer forward tokens/s (Mixtral-shaped bf16 layer, 1 GPU)"
     return f"MoE layer forward tokens/s ({spec.name})"
+
+
+def config_of(spec, world: int) -> dict:
+    w_b = accounting.W4_BYTES_PER_WEIGHT if spec.w4a16 else (2 if spec.dtype == "bf16" else 4)
+    return {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff, "E": spec.E,
+            "k": spec.k, "n_shared": spec.n_shared, "capacity_factor": spec.capacity_factor,
+            "weights": "w4a16 (int4 codes + fp32 scale per 128)" if spec.w4a16 else spec.dtype,
+            "l2": "no flush: weights of %.2f GB exceed the 126 MB L2"
+                  % (3 * spec.E * spec.d * spec.d_ff * w_b / 1e9),
+            "parallelism": f"replicas x{world}"}
 
 
 def host_layer(dev: dict) -> dict:
     return {k: (None if v is None else v.cpu()) for k, v in dev.items()}
 
 
-# ------------------------------------------------------------------ main
+def count_kernel_launches(torch, lay, x) -> int:
+    """Kernels one forward launches: the kernel nodes of a CUDA graph captured from it (-1 if
+    the graph cannot be inspected)."""
+    try:
+        from cuda.bindings import runtime as rt
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g):
+                lay.forward(x)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        raw = g.raw_cuda_graph()
+        graph = raw if isinstance(raw, rt.cudaGraph_t) else rt.cudaGraph_t(init_value=int(raw))
+        err, _, n = rt.cudaGraphGetNodes(graph, 0)
+        if err != rt.cudaError_t.cudaSuccess:
+            return -1
+        err, nodes, n = rt.cudaGraphGetNodes(graph, n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return -1
+        kernels = 0
+        for nd in nodes[:n]:
+            err, t = rt.cudaGraphNodeGetType(nd)
+            if err == rt.cudaError_t.cudaSuccess and t == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                kernels += 1
+        del g
+        return kernels
+    except Exception as e:   # noqa: BLE001 -- reported as unknown, never fatal to the bench
+        print(f"kernel count unavailable: {e}", file=sys.stderr)
+        return -1
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=moe_synth.MIXTRAL.name,
-                    choices=sorted(moe_synth.WORKLOADS))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--tokens", type=int, default=0,
-                    help="override the batch size N (smaller cases for profiling; not a bench line)")
-    ap.add_argument("--experts", type=int, default=0,
-                    help="override the expert count E (smaller cases for profiling; not a bench line)")
-    ap.add_argument("--backward", type=int, default=10,
-                    help="timed moe_backward iterations after the forward measurement (0: none)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="CPU-oracle budget for the cpu_baseline field (0 to skip)")
-    args = ap.parse_args()
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    spec = moe_synth.WORKLOADS[args.workload]
-    if args.tokens > 0:
-        spec = spec.with_(N=args.tokens, name=f"{spec.name}_N{args.tokens}")
-    if args.experts > 0:
-        spec = spec.with_(E=args.experts, k=min(spec.k, args.experts),
-                          name=f"{spec.name}_E{args.experts}")
-    peaks, peak_src = load_peaks()
+# ------------------------------------------------------------------ one workload
 
-    if args.impl == "reference":
-        return run_reference(args, spec, rank, world)
-
-    import torch
-    import torch.distributed as dist
+def measure(spec, args, peaks, torch, dist, world, rank, local, headline: bool):
+    """Device-timed forward of one workload: K steps after W warm-up steps, events around the
+    routed gate/up and down GEMMs of every timed step, clocks sampled during the region.
+    The headline workload also gets the end-to-end measurement and the CPU oracle leg."""
     from sparse_conditional_moe_b300 import moe
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = moe_synth.make_layer(spec, seed=0, device="cuda")
     cfg = moe.cfg_from_spec(spec)
     w4 = moe.quantize_layer_w4(dev) if spec.w4a16 else None
     host_copy = None
+    want_cpu = headline and rank == 0 and args.cpu_seconds > 0
     if w4 is not None:
         # the forward reads the 4-bit copies only: keep host bf16 weights for the oracle leg
-        # (if it runs) and free the device ones
-        if args.cpu_seconds > 0 and rank == 0:
+        if want_cpu:
             host_copy = host_layer(dev)
         for n in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
             if dev.get(n) is not None:
@@ -274,65 +363,77 @@ def main():
         lay.forward(xs[i % 2])
     torch.cuda.synchronize()
     if lay.device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"device error during warm-up ({spec.name})")
     st = lay.stats()
     kept_rows, touched = st["kept_rows"], st["touched_experts"]
 
     # ---------------- device-timed region (inputs resident in HBM)
-    # Each step records two events, around the routed gate/up GEMM (the dominant kernel, whose
-    # roofline is reported from these); the full per-phase breakdown comes from a separate
-    # traced pass, so seven event records per step do not add to the timed work of small,
-    # launch-bound layers.
+    # Each step records four events: around the routed gate/up GEMM (the dominant kernel, whose
+    # roofline is reported from these) and around the routed down GEMM.  The other per-phase
+    # times come from a separate traced pass.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gu_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-             for _ in range(args.steps)]
-    clocks = ClockSampler(gpu_id_for_smi(torch, local))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_uuid(torch, local))
     clocks.start()
-    time.sleep(0.15)
+    time.sleep(0.05)
     barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        lay.forward(xs[i % 2], events=[None, None, gu_ev[i][0], gu_ev[i][1], None, None, None])
+        lay.forward(xs[i % 2], events=[None, None, ev[i][0], ev[i][1], ev[i][2], None, None])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
+    region_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(region_ms, world, "cuda")
     if lay.device_error() != 0:
-        raise RuntimeError("device error during the timed region")
+        raise RuntimeError(f"device error during the timed region ({spec.name})")
     ms_step = elapsed_ms / args.steps
+    gu_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
 
     # ---------------- per-phase breakdown (traced pass, not part of the timed region)
-    trace_steps = max(1, min(args.steps, 50))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_TRACE_EVENTS)]
-          for _ in range(trace_steps)]
+    trace_steps = max(1, min(args.steps, 20))
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_TRACE_EVENTS)]
+           for _ in range(trace_steps)]
     for i in range(trace_steps):
-        lay.forward(xs[i % 2], events=ev[i])
+        lay.forward(xs[i % 2], events=tev[i])
     torch.cuda.synchronize()
-    value = job_rate(spec.N, world, ms_step)
-
     phases = ["route", "permute", "gateup", "down", "shared", "combine"]
-    ph_ms = {p: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(trace_steps))
+    ph_ms = {p: statistics.mean(tev[i][j].elapsed_time(tev[i][j + 1]) for i in range(trace_steps))
              for j, p in enumerate(phases)}
+    forked = (spec.dtype == "bf16" and spec.n_shared > 0 and spec.N <= SIDE_STREAM_MAX_TOKENS)
+    if forked or spec.n_shared == 0:
+        ph_ms.pop("shared")
 
-    # ---------------- roofline of the dominant kernel (routed gate/up grouped GEMM)
     act_b = 2 if spec.dtype == "bf16" else 4
     w_b = accounting.W4_BYTES_PER_WEIGHT if spec.w4a16 else act_b
-    gu_flops = accounting.gateup_flops(spec.d, spec.d_ff, kept_rows)
-    gu_ms_timed = statistics.mean(a.elapsed_time(b) for a, b in gu_ev)
-    gu_s = gu_ms_timed / 1e3
-    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    achieved_t = gu_flops / gu_s / 1e12
     work = accounting.layer_work(spec.N, spec.d, spec.d_ff, spec.E, spec.k, spec.n_shared,
                                  spec.d_ff_shared, act_b, kept_rows, touched, weight_bytes=w_b)
-    layer_tflops = work.flops / (ms_step / 1e3) / 1e12
-    layer_gbs = work.bytes / (ms_step / 1e3) / 1e9
     roof_s = work.roofline_s(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-    traffic = read_traffic("gateup", spec.name)
-    # the dominant kernel's rate from the timed region, the other phases from the traced pass
     phase_roof = phase_rooflines(spec, act_b, w_b, kept_rows, touched,
-                                 dict(ph_ms, gateup=gu_ms_timed), peaks)
+                                 dict(ph_ms, gateup=gu_ms, down=dn_ms), peaks)
+    out = {
+        "workload": spec.name, "value": job_rate(spec.N, world, ms_step), "unit": "tokens/s",
+        "ms_per_step": ms_step, "timed_region_ms": region_ms,
+        "layer": {"tflops": work.flops / (ms_step / 1e3) / 1e12,
+                  "hbm_gbs_alg": work.bytes / (ms_step / 1e3) / 1e9,
+                  "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s * 1e3 / ms_step,
+                  "bound": work.bound(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9),
+                  "kept_rows": kept_rows, "touched_experts": touched},
+        "gateup": phase_roof["gateup"], "down": phase_roof["down"],
+        "phase_ms": ph_ms, "phase_roofline": phase_roof,
+        "shared_phase": ("forked onto the library's side stream (overlaps the routed phases; "
+                         "not bracketed by the caller-stream events)") if forked else None,
+        "clocks": clk,
+    }
+    if not headline:
+        del lay, dev, xs, w4
+        torch.cuda.empty_cache()
+        return out
+
+    out["gpu_launches_per_step"] = count_kernel_launches(torch, lay, xs[0])
 
     # ---------------- end to end through the C ABI with host buffers
     # Every step copies its batch in from pinned host memory and its output back.  The copies run
@@ -343,7 +444,6 @@ def main():
     x_dev = [torch.empty_like(xs[0]) for _ in range(2)]
     out_dev = [torch.empty_like(lay.out) for _ in range(2)]
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    e2e_steps = max(3, min(args.steps, 50))
 
     def run_e2e(n):
         ev_in = [torch.cuda.Event() for _ in range(n)]
@@ -367,111 +467,42 @@ def main():
                 ev_d2h[i].record(down)
         return ev_d2h[n - 1]
 
-    run_e2e(3)
+    run_e2e(max(3, args.warmup))
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(up)
-    last = run_e2e(e2e_steps)
+    last = run_e2e(args.steps)
     down.wait_event(last)
     e1.record(down)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, "cuda")
-    e2e_value = job_rate(spec.N, world, e2e_ms)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
+    out["e2e"] = {"value": job_rate(spec.N, world, e2e_ms), "unit": "tokens/s",
+                  "h2d_bytes_per_step": x_host[0].numel() * x_host[0].element_size(),
+                  "d2h_bytes_per_step": out_host[0].numel() * out_host[0].element_size()}
 
-    # router 2, permute 4, m-tile plan 1 (not on the W4A16 path), routed 2, shared 2, combine 1
-    # ---------------- backward pass (bf16 layers whose fp32 weight gradients fit comfortably)
-    bwd = None
-    grad_bytes = 4.0 * (3 * spec.E * spec.d * spec.d_ff + 3 * spec.n_shared * spec.d * spec.d_ff_shared)
-    if (args.backward > 0 and not spec.w4a16 and spec.dtype == "bf16" and grad_bytes <= 24e9
-            and spec.d % 64 == 0 and spec.d_ff % 128 == 0):
-        dout = torch.randn(lay.out.shape, device="cuda").to(torch.bfloat16)
-        lay.forward(xs[0])
-        for _ in range(2):
-            lay.backward(dout)
-        torch.cuda.synchronize()
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for _ in range(args.backward):
-            lay.backward(dout)
-        b1.record(stream)
-        torch.cuda.synchronize()
-        if lay.device_error() != 0:
-            raise RuntimeError("device error in the backward pass")
-        bwd_ms = b0.elapsed_time(b1) / args.backward
-        # expert GEMM work of the backward: 2x the forward's (data and weight gradients)
-        bwd_flops = 2.0 * (accounting.gateup_flops(spec.d, spec.d_ff, kept_rows)
-                           + accounting.down_flops(spec.d, spec.d_ff, kept_rows)
-                           + 6.0 * spec.d * spec.d_ff_shared * spec.N * spec.n_shared)
-        bwd = {"ms": bwd_ms, "tokens_per_s": spec.N * world / (bwd_ms / 1e3),
-               "expert_tflops": bwd_flops / (bwd_ms / 1e3) / 1e12, "iterations": args.backward,
-               "note": "moe_backward after one forward, all gradients fp32; the expert GEMMs do 2x "
-                       "the forward's work (gate/up recomputed once more on top)"}
-
-    launches_per_step = 2 + 4 + (0 if spec.w4a16 else 1) + 2 + (2 if spec.n_shared > 0 else 0) + 1
-    gemm_kernel = ("grouped W4A16 gate/up SwiGLU (CUDA cores, FFMA2)" if spec.w4a16
-                   else "grouped gate/up SwiGLU GEMM (tcgen05)")
-
-    # ---------------- CPU oracle on a bounded sub-batch (rank 0 only)
-    cpu = None
-    if rank == 0 and args.cpu_seconds > 0:
-        rate, done, secs, sub, cores = cpu_oracle_rate(spec, host_copy or host_layer(dev),
-                                                       args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{done} tokens of {spec.name} in consecutive sub-batches of {sub} "
-                         f"(each its own batch), {secs:.1f} s of CPU work"
-                         + (" (weights quantised by the oracle beforehand, untimed)"
-                            if spec.w4a16 else "")}
-
-    if rank == 0:
-        line = {
-            "metric": metric_name(spec),
-            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if act_b == 2 else "f32",
-            "data": "synthetic (seeded N(0,1) activations, N(0,1/d_in) weights)",
-            "config": {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff,
-                       "E": spec.E, "k": spec.k, "n_shared": spec.n_shared,
-                       "capacity_factor": spec.capacity_factor,
-                       "weights": "w4a16 (int4 codes + fp32 scale per 128)" if spec.w4a16
-                       else spec.dtype,
-                       "l2": "no flush: weights of %.2f GB exceed the 126 MB L2" %
-                             (3 * spec.E * spec.d * spec.d_ff * w_b / 1e9),
-                       "parallelism": f"replicas x{world}"},
-            "layer": {"tflops": layer_tflops, "hbm_gbs_alg": layer_gbs,
-                      "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s * 1e3 / ms_step,
-                      "kept_rows": kept_rows, "touched_experts": touched,
-                      "gateup_ms_timed_region": gu_ms_timed, "phase_ms": ph_ms, "phase_roofline": phase_roof, "backward": bwd},
-            "roofline": ({"kernel": gemm_kernel, "bound": "tensor",
-                          "achieved": achieved_t, "peak": peak_t, "unit": "TFLOP/s",
-                          "frac": achieved_t / peak_t, "traffic": traffic,
-                          "frac_of_burst": achieved_t / peaks["bf16_tflops"],
-                          "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a "
-                                         f"continuous loop); burst {peaks['bf16_tflops']}"}
-                         if phase_roof["gateup"]["unit"] == "TFLOP/s" else
-                         {"kernel": gemm_kernel, "bound": "hbm",
-                          "achieved": phase_roof["gateup"]["achieved"], "peak": peaks["hbm_gbs"],
-                          "unit": "GB/s", "frac": phase_roof["gateup"]["frac"],
-                          "traffic": None if spec.w4a16 else traffic,
-                          "peak_source": f"{peak_src} HBM copy bandwidth"}),
-            "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": "tokens/s",
-                    "h2d_bytes_per_step": spec.N * spec.d * act_b,
-                    "d2h_bytes_per_step": spec.N * spec.d * act_b},
-            "gpu_launches": launches_per_step * args.steps,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    # ---------------- CPU oracle on a bounded sample (rank 0 only)
+    if want_cpu:
+        hl = host_copy or host_layer(dev)
+        del lay, dev, xs
+        torch.cuda.empty_cache()
+        rate, done, secs, sub, cores = cpu_oracle_rate(spec, hl, args.cpu_seconds)
+        out["cpu_baseline"] = {
+            "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} tokens of {spec.name} in {cpu_sample_note(spec, sub)}; "
+                      f"{secs:.1f} s of CPU work"
+                      + (" (weights quantised by the oracle beforehand, untimed)"
+                         if spec.w4a16 else "")}
+        out["cpu_baseline_one_core"] = cpu_oracle_one_core(spec, hl)
+    return out
 
 
 def phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks):
     """Achieved rate of every phase against its own bound (algorithmic work only): the GEMM
-    phases in TFLOP/s against the bf16 peak, the data-movement phases in GB/s against HBM.
+    phases in TFLOP/s against the burst bf16 peak, the data-movement phases in GB/s against HBM.
     w_b: bytes per expert weight (the activation size, or 0.53125 for W4A16)."""
     d, F, E, N, S, Fs = spec.d, spec.d_ff, spec.E, spec.N, spec.n_shared, spec.d_ff_shared
-    tf_peak, gb_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), peaks["hbm_gbs"]
+    tf_peak, gb_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
     w_bytes = w_b * d * F
     work = {
         # x read + W_r read
@@ -499,58 +530,165 @@ def phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks):
     return out
 
 
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("grouped_gemm_pair.cu", "tc_ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if its source hash is current."""
-    import hashlib
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary (scaled from
+    the captured case to the full launch), if the summary's source hash is current."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for f in ("grouped_gemm_tc.cu", "tc_ptx.cuh"):
-        h.update(open(os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", f), "rb").read())
-    h = h.hexdigest()[:16]
+    h = kernel_source_hash()
     for ln in open(path):
         parts = [p.strip() for p in ln.strip().strip("|").split("|")]
-        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == h:
+        if len(parts) >= 5 and parts[0] == kernel and parts[1] == workload and parts[2] == h:
             try:
-                return float(parts[3])
+                return float(parts[3]) * float(parts[4])
             except ValueError:
                 return None
     return None
 
 
+def roofline_of(spec, res, peaks, peak_src):
+    g = res["gateup"]
+    if g["unit"] == "TFLOP/s":
+        return {"kernel": "routed grouped gate/up SwiGLU GEMM (tcgen05, CTA pairs)",
+                "bound": "tensor", "achieved": g["achieved"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": g["achieved"] / peaks["bf16_tflops"],
+                "traffic": read_traffic("gateup", spec.name),
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM, best of 10)",
+                "ms_per_launch": g["ms"],
+                "work_per_launch": f"4*d*d_ff*kept_rows = "
+                                   f"{accounting.gateup_flops(spec.d, spec.d_ff, res['layer']['kept_rows']):.4g} flop"}
+    kern = ("routed grouped W4A16 gate/up SwiGLU (TMA + mma.sync)" if spec.w4a16
+            else "routed grouped gate/up SwiGLU GEMM (tcgen05, CTA pairs)")
+    return {"kernel": kern, "bound": "hbm", "achieved": g["achieved"], "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": g["frac"], "traffic": None if spec.w4a16 else
+            read_traffic("gateup", spec.name),
+            "peak_source": f"{peak_src} HBM copy bandwidth", "ms_per_launch": g["ms"]}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(moe_synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the batch size N (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count E (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure the named workload only (no `workloads` object)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU-oracle budget for the cpu_baseline field (0 to skip)")
+    args = ap.parse_args()
+    if args.impl == "ours" and args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = moe_synth.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        spec = spec.with_(N=args.tokens, name=f"{spec.name}_N{args.tokens}")
+    if args.experts > 0:
+        spec = spec.with_(E=args.experts, k=min(spec.k, args.experts),
+                          name=f"{spec.name}_E{args.experts}")
+    peaks, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        return run_reference(args, spec, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = measure(spec, args, peaks, torch, dist, world, rank, local, headline=True)
+    side = {}
+    if not args.no_workloads and args.tokens == 0 and args.experts == 0:
+        for s in SIDE_WORKLOADS:
+            if s.name == spec.name:
+                continue
+            r = measure(s, args, peaks, torch, dist, world, rank, local, headline=False)
+            side[s.name] = {"ms_per_step": r["ms_per_step"], "value": r["value"],
+                            "unit": "tokens/s", "gateup": r["gateup"], "down": r["down"],
+                            "layer_roofline_frac": r["layer"]["roofline_frac"],
+                            "layer_bound": r["layer"]["bound"],
+                            "kept_rows": r["layer"]["kept_rows"],
+                            "touched_experts": r["layer"]["touched_experts"],
+                            "phase_ms": r["phase_ms"], "shared_phase": r["shared_phase"],
+                            "clocks": {k: r["clocks"].get(k) for k in
+                                       ("sm_mhz", "sm_min_mhz", "samples", "reasons")},
+                            "config": config_of(s, world)}
+
+    if rank == 0:
+        per_step = res.get("gpu_launches_per_step", -1)
+        line = {
+            "metric": metric_name(spec),
+            "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if spec.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/d_in) weights)",
+            "config": config_of(spec, world),
+            "layer": dict(res["layer"], phase_ms=res["phase_ms"],
+                          phase_roofline=res["phase_roofline"], shared_phase=res["shared_phase"],
+                          timed_region_ms=res["timed_region_ms"]),
+            "roofline": roofline_of(spec, res, peaks, peak_src),
+            "clocks": res["clocks"],
+            "e2e": res["e2e"],
+            "gpu_launches": per_step * args.steps if per_step > 0 else None,
+            "gpu_launches_per_step": per_step,
+            "cpu_baseline": res.get("cpu_baseline"),
+            "cpu_baseline_one_core": res.get("cpu_baseline_one_core"),
+            "workloads": side or None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_reference(args, spec, rank, world):
-    """The CPU oracle timed on this machine's host cores on the same workload and metric."""
+    """The CPU oracle timed on this machine's host cores on the same workload and metric.  Each step
+    is one sub-batch of the workload (as many tokens as the box has cores, routed as a batch of
+    its own); ms_per_step is the measured time of one such step."""
     if rank != 0:
         return
-    import torch
     layer = moe_synth.make_layer(spec, seed=0, device="cpu")
-    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_oracle_rate(spec, layer, 0.0, max_steps=1)
-    rates = []
-    t0 = time.perf_counter()
-    total, secs_total = 0, 0.0
+    step_s, total = [], 0
+    sub = cores = 0
     for _ in range(args.steps):
-        rate, done, secs, sub, cores = cpu_oracle_rate(spec, layer, budget)
+        t0 = time.perf_counter()
+        rate, done, secs, sub, cores = cpu_oracle_rate(spec, layer, 0.0, max_steps=1)
+        step_s.append(time.perf_counter() - t0)
         total += done
-        secs_total += secs
-    wall = time.perf_counter() - t0
-    value = total / secs_total
+    value = total / sum(step_s)
     line = {
         "impl": "reference", "metric": metric_name(spec), "value": value,
         "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * spec.N / value, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": spec.name, "N": spec.N, "d": spec.d, "d_ff": spec.d_ff,
-                   "E": spec.E, "k": spec.k},
+        "ms_per_step": 1e3 * statistics.mean(step_s), "tokens_per_step": sub,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle experts, fp32 router)", "data": "synthetic",
+        "config": config_of(spec, 1),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{total} tokens in sub-batches of {sub}, {secs_total:.1f} s "
-                                   f"of oracle time ({wall:.1f} s wall)"},
+                         "sample": f"{total} tokens of {spec.name}: {args.steps} steps, each "
+                                   f"{cpu_sample_note(spec, sub)}"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    del torch
     print(json.dumps(line), flush=True)
 
 

@@ -1,5 +1,6 @@
-"""The benchmark fills roofline.traffic from the committed per-layer ncu table only while the
-table's source hash matches the kernel source, and only for the layer it was captured on."""
+"""The benchmark fills roofline.traffic from the committed ncu table only while the table's
+source hash matches the kernel source, only for the layer it was captured for, and scaled from
+the captured case to a full launch by the table's factor."""
 import hashlib
 import os
 import shutil
@@ -10,18 +11,17 @@ sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
 
-SRC = ("grouped_gemm_tc.cu", "tc_ptx.cuh")
+SRC = ("grouped_gemm_pair.cu", "tc_ptx.cuh")
+HEAD = ("| kernel | workload | source hash | dram bytes per captured launch | scale to full launch |\n"
+        "|---|---|---|---|---|\n")
 
 
-def _tree(tmp_path, table_hash):
+def _tree(tmp_path):
     csrc = tmp_path / "sparse_conditional_moe_b300" / "csrc"
     csrc.mkdir(parents=True)
     for f in SRC:
         shutil.copy(os.path.join(ROOT, "sparse_conditional_moe_b300", "csrc", f), csrc / f)
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "ncu_traffic.md").write_text(
-        "| kernel | workload | source hash | dram bytes per launch |\n|---|---|---|---|\n"
-        f"| gateup | layer_a | {table_hash} | 1.5e9 |\n")
     return csrc
 
 
@@ -33,15 +33,15 @@ def _hash(csrc):
 
 
 def test_traffic_read_only_for_current_source_and_its_layer(tmp_path, monkeypatch):
-    csrc = _tree(tmp_path, "0" * 16)
+    csrc = _tree(tmp_path)
     good = _hash(csrc)
     (tmp_path / "profiles" / "ncu_traffic.md").write_text(
-        "| kernel | workload | source hash | dram bytes per launch |\n|---|---|---|---|\n"
-        f"| gateup | layer_a | {good} | 1.5e9 |\n")
+        HEAD + f"| gateup | layer_a | {good} | 1.5e9 | 8 |\n"
+               f"| gateup | layer_c | {'0' * 16} | 2.0e9 | 1 |\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.read_traffic("gateup", "layer_a") == 1.5e9
+    assert bench.read_traffic("gateup", "layer_a") == 1.5e9 * 8
     assert bench.read_traffic("gateup", "layer_b") is None
+    assert bench.read_traffic("gateup", "layer_c") is None      # stale hash
     # any change to the kernel source retires the captured number
-    (csrc / "grouped_gemm_tc.cu").write_text((csrc / "grouped_gemm_tc.cu").read_text() + "\n")
+    (csrc / "grouped_gemm_pair.cu").write_text((csrc / "grouped_gemm_pair.cu").read_text() + "\n")
     assert bench.read_traffic("gateup", "layer_a") is None
-

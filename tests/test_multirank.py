@@ -62,3 +62,27 @@ def test_reference_arm_prints_only_on_rank_zero():
                        timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank_zero():
+    """The reference arm (the CPU oracle) prints one line whose config equals our arm's, whose
+    steps each take the measured time it reports, and whose tokens per step are stated."""
+    sys.path.insert(0, ROOT)
+    import json
+    import time
+
+    import bench
+    import moe_synth
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    t0 = time.perf_counter()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_fp32", "--steps", "3", "--warmup", "1"], env=env,
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    wall = time.perf_counter() - t0
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 3
+    assert line["config"] == bench.config_of(moe_synth.TINY, 1)
+    assert line["steps"] * line["ms_per_step"] / 1e3 <= wall
+    assert line["tokens_per_step"] >= 1
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
