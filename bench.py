@@ -55,6 +55,42 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 
+class _Nvml:
+    """The few NVML calls the clock sampler needs, through ctypes on the driver's libnvidia-ml."""
+
+    def __init__(self, uuid: str):
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        self.L = L
+        rc = (getattr(L, "nvmlInit_v2", None) or L.nvmlInit)()
+        if rc != 0:
+            raise RuntimeError(f"nvmlInit returned {rc}")
+        self.h = ctypes.c_void_p()
+        rc = L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError(f"nvmlDeviceGetHandleByUUID({uuid}) returned {rc}")
+        self._reasons = (getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                         or L.nvmlDeviceGetCurrentClocksThrottleReasons)
+        self.max_mhz = self.clock(getattr(L, "nvmlDeviceGetMaxClockInfo"))
+
+    def clock(self, fn=None) -> float:
+        v = ctypes.c_uint()
+        rc = (fn or self.L.nvmlDeviceGetClockInfo)(self.h, 1, ctypes.byref(v))   # 1 = SM clock
+        if rc != 0:
+            raise RuntimeError(f"clock query returned {rc}")
+        return float(v.value)
+
+    def sample(self):
+        mw, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.L.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw)) != 0:
+            mw.value = 0
+        if self._reasons(self.h, ctypes.byref(rs)) != 0:
+            rs.value = 0
+        return self.clock(), mw.value / 1000.0, int(rs.value)
+
+    def close(self):
+        self.L.nvmlShutdown()
+
+
 class ClockSampler:
     """SM clocks and throttle reasons sampled every few milliseconds during a timed region,
     through NVML (nvidia-smi polling as a fallback)."""
@@ -69,18 +105,11 @@ class ClockSampler:
         self._thread = None
         self._nvml = None
         self._proc = None
+        self.nvml_error = None
 
     def start(self):
-        self.nvml_error = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            try:
-                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
-            except Exception:   # noqa: BLE001 -- older bindings want bytes
-                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid.encode())
-            self._nvml = (pynvml, h)
-            self._max = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._nvml = _Nvml(self.uuid)
         except Exception as e:   # noqa: BLE001 -- fall back to nvidia-smi polling
             self.nvml_error = f"{type(e).__name__}: {e}"
             self._nvml = None
@@ -101,21 +130,13 @@ class ClockSampler:
         except (OSError, ValueError):
             self._proc = None
 
-    def _reasons(self, h):
-        pynvml = self._nvml[0]
-        f = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
-        return f(h)
-
     def _poll(self):
-        pynvml, h = self._nvml
+        nv = self._nvml
         while not self._stop.is_set():
             try:
-                sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                pw = pynvml.nvmlDeviceGetPowerUsage(h) / 1000.0
-                rs = self._reasons(h)
-                self.samples.append((float(sm), float(self._max), pw, int(rs)))
-            except Exception:
+                sm, pw, rs = nv.sample()
+                self.samples.append((sm, nv.max_mhz, pw, rs))
+            except Exception:   # noqa: BLE001 -- a failed poll is a missing sample
                 pass
             time.sleep(self.period)
 
@@ -142,20 +163,23 @@ class ClockSampler:
             self._thread.join(timeout=2)
         if self._nvml is not None:
             try:
-                self._nvml[0].nvmlShutdown()
-            except Exception:
+                self._nvml.close()
+            except Exception:   # noqa: BLE001
                 pass
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
-                    "reasons": ["no clock samples (NVML and nvidia-smi unavailable)"]}
+            out = {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                   "reasons": ["no clock samples (NVML and nvidia-smi unavailable)"]}
+            if self.nvml_error:
+                out["nvml_error"] = self.nvml_error
+            return out
         reasons = sorted({n for n, b in self.REASONS for s in self.samples if s[3] & b})
         out = {"sm_mhz": statistics.median(s[0] for s in self.samples),
-                "sm_min_mhz": min(s[0] for s in self.samples),
-                "sm_max_mhz": max(s[1] for s in self.samples),
-                "power_w_max": max(s[2] for s in self.samples),
-                "samples": len(self.samples),
-                "source": "nvml" if self._nvml is not None else "nvidia-smi",
-                "reasons": reasons}
+               "sm_min_mhz": min(s[0] for s in self.samples),
+               "sm_max_mhz": max(s[1] for s in self.samples),
+               "power_w_max": max(s[2] for s in self.samples),
+               "samples": len(self.samples),
+               "source": "nvml" if self._nvml is not None else "nvidia-smi",
+               "reasons": reasons}
         if self.nvml_error:
             out["nvml_error"] = self.nvml_error
         return out

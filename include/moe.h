@@ -97,6 +97,22 @@ MOE_API moe_status moe_workspace_init(const moe_cfg *cfg, void *ws, size_t ws_by
 /* Rows of the expert-grouped buffers: min(N*k, E*C) (N*k without capacity). */
 MOE_API int64_t moe_grouped_rows(const moe_cfg *cfg);
 
+/*
+ * moe_router_prepare -- prepares the router weight once for many calls ("混合专家 MoE", 实现
+ * section, MoE.route: the router is a fixed linear layer d -> E between weight updates).  For
+ * bf16 layers with E > 32 the router runs on the tensor cores on an exact three-way bf16 split
+ * of the fp32 W_r (hi + mid + lo == W_r bit for bit); this call writes that split into the
+ * workspace and records, in host memory, that the workspace now holds the split of this W_r
+ * pointer.  moe_route, moe_forward and moe_forward_traced called with the same workspace and
+ * the same W_r pointer then skip the split.  Other layers: nothing to prepare (MOE_OK).
+ *   W_r [E,d] fp32 in (device); ws as for moe_forward; asynchronous on stream.
+ * The caller must call it again after changing W_r's contents (the record is keyed on the
+ * pointer, not the values); moe_workspace_init forgets the record.  Calls that pass another
+ * W_r pointer split their own weight as usual.
+ */
+MOE_API moe_status moe_router_prepare(const moe_cfg *cfg, const float *W_r, void *ws,
+                                      size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------------ steps */
 
 /*

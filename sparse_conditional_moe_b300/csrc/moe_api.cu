@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -263,6 +264,28 @@ moe_status do_shared_and_combine(const moe_cfg* c, const void* y_perm, const int
     return MOE_OK;
 }
 
+// ------------------------------------------------------------------ prepared router splits
+//
+// moe_router_prepare records, per workspace, the W_r pointer (and E, d) whose exact bf16 split
+// sits in the workspace; forwards and routes that pass the same pointer skip the split.
+struct PreparedSplit {
+    const float* W_r;
+    int E, d;
+};
+std::mutex g_prepared_mu;
+std::unordered_map<uintptr_t, PreparedSplit> g_prepared;
+
+bool split_prepared(const moe_cfg& c, const float* W_r, const void* ws) {
+    std::lock_guard<std::mutex> lock(g_prepared_mu);
+    auto it = g_prepared.find(reinterpret_cast<uintptr_t>(ws));
+    return it != g_prepared.end() && it->second.W_r == W_r && it->second.E == c.E &&
+           it->second.d == c.d;
+}
+void forget_prepared(const void* ws) {
+    std::lock_guard<std::mutex> lock(g_prepared_mu);
+    g_prepared.erase(reinterpret_cast<uintptr_t>(ws));
+}
+
 // ------------------------------------------------------------------ side stream
 //
 // For a decode-sized batch the shared experts are a handful of tiles that would run alone with
@@ -436,7 +459,24 @@ moe_status moe_workspace_size(const moe_cfg* cfg, size_t* bytes) {
 moe_status moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    forget_prepared(ws);
     MOE_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_router_prepare(const moe_cfg* cfg, const float* W_r, void* ws, size_t ws_bytes,
+                              void* stream) {
+    NvtxRange nvtx_("moe_router_prepare");
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    MOE_TRY(need(W_r, 16));
+    if (!router_uses_tensor_cores(*cfg)) return MOE_OK;
+    const WsLayout L = ws_layout(*cfg);
+    forget_prepared(ws);
+    MOE_CUDA(tc_router_split(W_r, cfg->E, cfg->d, at<__nv_bfloat16>(ws, L.router_w3),
+                             (cudaStream_t)stream));
+    std::lock_guard<std::mutex> lock(g_prepared_mu);
+    g_prepared[reinterpret_cast<uintptr_t>(ws)] = PreparedSplit{W_r, cfg->E, cfg->d};
     return MOE_OK;
 }
 
@@ -455,10 +495,12 @@ moe_status moe_route(const moe_cfg* cfg, const void* x, const float* W_r, const 
     MOE_TRY(need(P_sum, 4));
     if (cfg->bias_mode != 0) MOE_TRY(need(b_r, 4));
     const WsLayout L = ws_layout(*cfg);
+    const bool prepared = split_prepared(*cfg, W_r, ws);
+    if (!prepared) forget_prepared(ws);
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, idx, w, gap, at<float>(ws, L.lse),
                            at<float>(ws, L.p_part), P_sum,
                            at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits),
-                           at<int32_t>(ws, L.err), (cudaStream_t)stream));
+                           at<int32_t>(ws, L.err), (cudaStream_t)stream, nullptr, prepared));
     return MOE_OK;
 }
 
@@ -547,6 +589,9 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev && ev[0]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    // a forward that splits W_r itself overwrites the workspace's prepared split
+    const bool prepared = split_prepared(*cfg, W_r, ws);
+    if (!prepared) forget_prepared(ws);
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
     cudaEvent_t join = nullptr;
     if (side) {
@@ -556,7 +601,8 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
-                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
+                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s,
+                           nullptr, prepared));
     if (ev && ev[1]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
                             at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
@@ -633,6 +679,9 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     const WsLayout L = ws_layout(*cfg);
     int32_t* err = at<int32_t>(ws, L.err);
     if (ev && ev[0]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[0], s));
+    // a forward that splits W_r itself overwrites the workspace's prepared split
+    const bool prepared = split_prepared(*cfg, W_r, ws);
+    if (!prepared) forget_prepared(ws);
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
     cudaEvent_t join = nullptr;
     if (side) {
@@ -642,7 +691,8 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
                            at<float>(ws, L.gap), at<float>(ws, L.lse), at<float>(ws, L.p_part),
                            at<float>(ws, L.P_sum),
-                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s));
+                           at<__nv_bfloat16>(ws, L.router_w3), at<float>(ws, L.logits), err, s,
+                           nullptr, prepared));
     if (ev && ev[1]) MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[1], s));
     MOE_CUDA(launch_permute(*cfg, at<int32_t>(ws, L.idx), at<float>(ws, L.w), x,
                             at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
@@ -709,6 +759,7 @@ moe_status moe_backward(const moe_cfg* cfg, const void* x, const float* W_r, con
         MOE_TRY(need(dx, 16));
     }
     const WsLayout L = ws_layout(*cfg);
+    forget_prepared(ws);   // the backward's router pass re-splits W_r into the workspace
     BwdArgs a{};
     a.cfg = cfg;
     a.x = x;

@@ -52,18 +52,29 @@ WsLayout ws_layout(const moe_cfg& c);
 
 // lse [N] (nullable): log-sum-exp of each token's logits, for the z-loss; probs [N, E]
 // (nullable): the softmax probabilities, for the backward pass.
+// w3_ready: the tensor-core router's weight split in w3 is current (moe_router_prepare).
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* lse, float* p_part,
                           float* P_sum, __nv_bfloat16* w3, float* logits, int32_t* err,
-                          cudaStream_t s, float* probs = nullptr);
+                          cudaStream_t s, float* probs = nullptr, bool w3_ready = false);
 
-// Tensor-core router logits [N, E] (fp32) for bf16 x (see router_tc.cu).
-// Tensor-core router: number of CTA groups that split d (1 = none; small N only) and the floats
-// its logits region needs (the logits, plus one [N, E] slice sum per 256 of d when split).
+// Tensor-core router for bf16 x (see router_tc.cu).  w3 holds the exact hi/mid/lo bf16 split of
+// W_r [3, E, d] (tc_router_split writes it).  router_tc_split: number of CTA groups that split d
+// (1 = none; small N only); router_tc_logits_floats: the floats its unfused logits region needs
+// (the logits, plus one [N, E] slice sum per 256 of d when split); router_tc_fused: whether the
+// fused kernel (softmax and top-k in the same launch, logits kept on chip) applies;
+// router_tc_part_rows: the probability-sum rows the fused kernel writes.
 int router_tc_split(int64_t N, int d, int E);
 size_t router_tc_logits_floats(int64_t N, int d, int E);
-cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
-                             __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s);
+bool router_tc_fused(int64_t N, int d, int E);
+int router_tc_part_rows(int64_t N, int E);
+cudaError_t tc_router_split(const float* W_r, int E, int d, __nv_bfloat16* w3, cudaStream_t s);
+cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const __nv_bfloat16* w3,
+                             int E, float* logits, int32_t* err, cudaStream_t s);
+cudaError_t tc_router_fused(const __nv_bfloat16* x, int64_t N, int d, const __nv_bfloat16* w3,
+                            int E, const float* b_r, int bias_mode, int k, int renorm,
+                            int32_t* idx, float* w, float* gap, float* lse, float* probs,
+                            float* p_part, int32_t* err, cudaStream_t s);
 
 cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w, const void* x,
                            int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_off,

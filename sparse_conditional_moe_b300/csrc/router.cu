@@ -8,9 +8,10 @@
 // Three ways to get the logits, one epilogue:
 //   E <= 32      router_gemv_kernel: a warp per two tokens, lanes split d in 8-wide chunks,
 //                each lane accumulates E short fp32 chains, a butterfly shuffle sums them;
-//   E > 32, bf16 the tensor-core router of router_tc.cu writes fp32 logits [N, E] (split
-//                over d for small N), then logits_topk_kernel finishes each token, one per
-//                warp;
+//   E > 32, bf16 the tensor-core router of router_tc.cu: for E <= 512 and batches whose d is
+//                not split, one fused launch (logits on chip, the tokens finished by the
+//                cluster of expert-block CTAs); otherwise fp32 logits [N, E] (split over d for
+//                small N), then logits_topk_kernel finishes each token, one per warp;
 //   E > 32, fp32 router_tiled_kernel: BT tokens x all experts per block, DK-wide slices of x
 //                and W_r in shared memory, each slice an fp32 FMA chain, slices added to the
 //                running logit with compensated (Kahan) summation.
@@ -19,13 +20,12 @@
 // (probability desc, expert index asc) -- each lane sorts its candidates once and offers its
 // head, two warp reductions pick the winner; the (k+1)-th gives the near-tie gap; per-block
 // column sums of the probabilities go to p_part (deterministic, no float atomics).
-#include <float.h>
-#include <limits.h>
-
-#include "moe_internal.cuh"
+#include "router_finish.cuh"
 
 namespace moe {
 namespace {
+
+using namespace router_detail;
 
 constexpr int kRouterThreads = 256;
 constexpr int kWarps = kRouterThreads / 32;
@@ -33,170 +33,6 @@ constexpr int kWarps = kRouterThreads / 32;
 __device__ __forceinline__ float load_x(const float* x, int64_t i) { return x[i]; }
 __device__ __forceinline__ float load_x(const __nv_bfloat16* x, int64_t i) {
     return __bfloat162float(x[i]);
-}
-
-// Unsigned key with the order of the float (negative floats bit-flipped, -0 made +0); a NaN
-// gets the lowest key, so like the comparisons it stands for it never wins over a number.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    const float f = v == 0.f ? 0.f : v;
-    const uint32_t u = __float_as_uint(f);
-    return (f != f) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Warp arg-max over (value desc, index asc); every lane ends with the same pair: the maximum key
-// is one warp reduction and the lowest index among the lanes holding it a second.
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-    const uint32_t key = order_key(v);
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
-    i = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)i : 0xffffffffu);
-    v = key_value(mk);
-}
-
-// Softmax, top-k, gap and renormalisation of one token held by one warp.  v[i] is the logit of
-// expert lane + 32 i (ignored for experts >= E).  Adds the probabilities into pacc.
-// bias_mode 1: b_r is added to the logits; 2: the top-k is chosen on p + b_r (rounded once to
-// fp32) while the weights and probabilities stay unbiased ("混合专家 MoE", 负载均衡: the
-// DeepSeek-V3 bias only picks the experts).
-template <int NV>
-__device__ __forceinline__ void finish_token(float (&v)[NV], const float* __restrict__ b_r,
-                                             int bias_mode, int E, int k, int renorm, int64_t tok,
-                                             int32_t* __restrict__ idx_out,
-                                             float* __restrict__ w_out,
-                                             float* __restrict__ gap_out,
-                                             float* __restrict__ lse_out,
-                                             float* __restrict__ probs_out, float (&pacc)[NV]) {
-    const int lane = threadIdx.x & 31;
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            if (bias_mode == 1) v[i] += b_r[e];
-            m = fmaxf(m, v[i]);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = lane + 32 * i;
-        v[i] = (e < E) ? expf(v[i] - m) : 0.f;
-        s += v[i];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0 && lse_out) lse_out[tok] = m + logf(s);   // log-sum-exp of the logits (z-loss)
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = lane + 32 * i;
-        v[i] = (e < E) ? v[i] / s : -1.f;   // -1: never selected
-        if (e < E) pacc[i] += v[i];
-        if (e < E && probs_out) probs_out[tok * E + e] = v[i];
-    }
-    // selection scores: the probabilities, or p + b for the selection-only bias
-    float sv[NV];
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = lane + 32 * i;
-        sv[i] = (bias_mode == 2 && e < E) ? v[i] + b_r[e] : v[i];
-    }
-    float my_val = 0.f, kth = 0.f, sel_sum = 0.f;
-    int my_idx = 0;
-    const int rounds = k < E ? k + 1 : k;
-    if constexpr (NV <= 8) {
-        // Each lane sorts its NV candidates once by (score desc, expert asc); every round the
-        // lanes offer their heads, two warp reductions pick the winner (the same order as a
-        // full arg-max over the untaken experts) and the winning lane pops its head.
-        uint32_t key[NV];
-        int ex[NV];
-        float pr[NV];
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            const int e = lane + 32 * i;
-            key[i] = e < E ? order_key(sv[i]) : 0u;
-            ex[i] = e < E ? e : INT_MAX;
-            pr[i] = v[i];
-        }
-#pragma unroll
-        for (int a = 1; a < NV; a++)
-#pragma unroll
-            for (int b = a; b > 0; b--)
-                if (key[b] > key[b - 1]) {   // strict: equal keys keep the lower expert first
-                    const uint32_t tk = key[b]; key[b] = key[b - 1]; key[b - 1] = tk;
-                    const int te = ex[b]; ex[b] = ex[b - 1]; ex[b - 1] = te;
-                    const float tp = pr[b]; pr[b] = pr[b - 1]; pr[b - 1] = tp;
-                }
-        for (int j = 0; j < rounds; j++) {
-            const uint32_t mk = __reduce_max_sync(0xffffffffu, key[0]);
-            const int bi =
-                (int)__reduce_min_sync(0xffffffffu, key[0] == mk ? (uint32_t)ex[0] : 0xffffffffu);
-            const float bv = key_value(mk);
-            if (j < k) {
-                const int wl = bi & 31;
-                const float pv = __shfl_sync(0xffffffffu, pr[0], wl);
-                const bool pop = lane == wl;
-#pragma unroll
-                for (int i = 0; i + 1 < NV; i++) {
-                    key[i] = pop ? key[i + 1] : key[i];
-                    ex[i] = pop ? ex[i + 1] : ex[i];
-                    pr[i] = pop ? pr[i + 1] : pr[i];
-                }
-                if (pop) {
-                    key[NV - 1] = 0u;
-                    ex[NV - 1] = INT_MAX;
-                }
-                if (lane == j) {
-                    my_val = pv;
-                    my_idx = bi;
-                }
-                sel_sum += pv;   // slot order, identical on every lane
-                kth = bv;
-            } else if (lane == 0 && gap_out) {
-                gap_out[tok] = kth - bv;
-            }
-        }
-    } else {
-    uint32_t taken = 0;
-    for (int j = 0; j < rounds; j++) {
-        float bv = -FLT_MAX;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            const int e = lane + 32 * i;
-            if (e < E && !(taken & (1u << i)) && (sv[i] > bv || (sv[i] == bv && e < bi))) {
-                bv = sv[i];
-                bi = e;
-            }
-        }
-        warp_argmax(bv, bi);
-        if (j < k) {
-            // the probability of the chosen expert, from the lane that holds it
-            float pv = 0.f;
-#pragma unroll
-            for (int i = 0; i < NV; i++)
-                if (i == (bi >> 5)) pv = v[i];
-            pv = __shfl_sync(0xffffffffu, pv, bi & 31);
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == j) {
-                my_val = pv;
-                my_idx = bi;
-            }
-            sel_sum += pv;   // slot order, identical on every lane
-            kth = bv;
-        } else if (lane == 0 && gap_out) {
-            gap_out[tok] = kth - bv;
-        }
-    }
-    }
-    if (k >= E && lane == 0 && gap_out) gap_out[tok] = __int_as_float(0x7f800000);
-    if (lane < k) {
-        idx_out[tok * k + lane] = my_idx;
-        w_out[tok * k + lane] = renorm ? my_val / sel_sum : my_val;
-    }
 }
 
 // Column sums of the probabilities of this block's tokens, combined across warps in warp order.
@@ -549,13 +385,23 @@ int64_t router_part_rows(int64_t N) { return (N + 7) / 8 + 1; }
 cudaError_t launch_router(const moe_cfg& c, const void* x, const float* W_r, const float* b_r,
                           int32_t* idx, float* w, float* gap, float* lse, float* p_part,
                           float* P_sum, __nv_bfloat16* w3, float* logits, int32_t* err,
-                          cudaStream_t s, float* probs) {
+                          cudaStream_t s, float* probs, bool w3_ready) {
     const float* bias = c.bias_mode != 0 ? b_r : nullptr;
     int blocks = 0;
     if (c.N > 0) {
         if (router_uses_tensor_cores(c)) {
-            cudaError_t e = tc_router_logits((const __nv_bfloat16*)x, c.N, c.d, W_r, c.E, w3,
-                                             logits, err, s);
+            cudaError_t e = cudaSuccess;
+            if (!w3_ready) e = tc_router_split(W_r, c.E, c.d, w3, s);
+            if (e != cudaSuccess) return e;
+            if (router_tc_fused(c.N, c.d, c.E)) {
+                e = tc_router_fused((const __nv_bfloat16*)x, c.N, c.d, w3, c.E, bias, c.bias_mode,
+                                    c.k, c.renorm, idx, w, gap, lse, probs, p_part, err, s);
+                if (e != cudaSuccess) return e;
+                reduce_p_kernel<<<(c.E + 31) / 32, 1024, 0, s>>>(
+                    p_part, router_tc_part_rows(c.N, c.E), c.E, P_sum);
+                return cudaGetLastError();
+            }
+            e = tc_router_logits((const __nv_bfloat16*)x, c.N, c.d, w3, c.E, logits, err, s);
             if (e != cudaSuccess) return e;
             switch (pad_experts(c.E) / 32) {
                 case 1: case 2: blocks = launch_topk<2>(c, logits, bias, idx, w, gap, lse, probs, p_part, s); break;

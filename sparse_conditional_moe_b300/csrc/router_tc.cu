@@ -18,10 +18,20 @@
 //   warp 1      TMEM allocation (512 columns: two 192-column slice accumulators) and the
 //               single MMA-issuing thread (tcgen05.mma M=128, N=192, K=16);
 //   warps 2..9  two epilogue warpgroups, experts [0,32) and [32,64) of the tile.
-// Logits are written as fp32 [N, E]; softmax and top-k follow in router.cu.
-// Small batches (N <= 1024, few CTAs) split d over blockIdx.z: each CTA writes the sum of every
+// Fused form (d not split, 192 < E <= 512): the ceil(E/64) CTAs of one token tile run as a
+// thread-block cluster.  Each CTA leaves its 128 x 64 logits in its shared memory (the drained ring); after a
+// cluster barrier every CTA finishes 128 / cluster-size of the tile's tokens -- softmax, top-k,
+// gap and renormalisation as in router.cu, one warp per token, all ten warps -- reading the
+// token's E logits from the cluster's shared memory, and writes its column sums of the
+// probabilities.  The logits never go to global memory.  A warp finishes a token in a chain of
+// dependent shuffles and reductions (about a microsecond), so the fused form pays off only while a
+// CTA finishes few tokens: with clusters of 2 (E <= 128, 64 tokens per CTA) the separate top-k
+// kernel, whose thousands of warps hide that latency, is faster and is used instead.
+// Unfused form: logits are written as fp32 [N, E] and router.cu finishes the tokens.  Small
+// batches (N <= 1024, few CTAs) split d over blockIdx.z: each CTA writes the sum of every
 // 256-wide slice it covers, and router_slices_kernel adds the slices in order with the same
 // Kahan recurrence, so the logits are bit-identical to the unsplit kernel's.
+#include "router_finish.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -42,6 +52,28 @@ constexpr int RSTAGE = RA_STAGE + RB_STAGE;
 constexpr int RTHREADS = 320;
 constexpr uint32_t RTMEM_COLS = 512;
 constexpr int RSMEM = RSTAGES * RSTAGE + 1024 + 256;
+constexpr int LS_STRIDE = REN + 1;        // fused: logits [128][65] fp32 in the drained ring
+constexpr int kFinishWarps = RTHREADS / 32;   // fused: every warp finishes tokens
+static_assert(RBM * LS_STRIDE * 4 + kFinishWarps * 512 * 4 <= RSTAGES * RSTAGE,
+              "fused finish buffers fit the ring");
+
+// The fused router's per-token outputs (see launch_router for their meaning).
+struct RouterFinish {
+    const float* b_r;
+    int bias_mode, k, renorm;
+    int32_t* idx;
+    float* w;
+    float* gap;
+    float* lse;
+    float* probs;
+    float* p_part;
+};
+
+static __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 __global__ void split3_kernel(const float* __restrict__ W, int64_t n, __nv_bfloat16* __restrict__ out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -57,10 +89,12 @@ __global__ void split3_kernel(const float* __restrict__ W, int64_t n, __nv_bfloa
     }
 }
 
+// FNV = 0: logits to global memory; FNV > 0: fused finish, expert slots per lane = FNV.
+template <int FNV>
 __global__ void __launch_bounds__(RTHREADS, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                  int64_t N, int d, int E, int slices_per_cta, float* __restrict__ logits,
-                 float* __restrict__ slice_out, int32_t* err) {
+                 float* __restrict__ slice_out, int32_t* err, const RouterFinish fin) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -234,7 +268,12 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         }
         const int64_t tok = (int64_t)m0 + row;
         const int ebase = e0 + wg * 32;
-        if (ok && !slice_out && tok < N) {
+        if (FNV > 0) {
+            // the ring is drained (every MMA that read it has completed): the logits go there
+            float* Ls = reinterpret_cast<float*>(smem);
+#pragma unroll
+            for (int j = 0; j < 32; j++) Ls[row * LS_STRIDE + wg * 32 + j] = acc[j];
+        } else if (ok && !slice_out && tok < N) {
             float* dst = logits + tok * E + ebase;
             if (ebase + 32 <= E && (E & 3) == 0) {
 #pragma unroll
@@ -253,6 +292,49 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, RTMEM_COLS);
+    }
+    if constexpr (FNV > 0) {
+        // every CTA of the cluster holds its experts' logits for the tile's 128 tokens
+        cluster_sync_all();
+        const int cy = (int)gridDim.y;                 // the cluster spans the expert blocks
+        const int per = (RBM + cy - 1) / cy;
+        const int t_beg = (int)blockIdx.y * per;
+        const int t_end = min(RBM, t_beg + per);
+        float* ptab = reinterpret_cast<float*>(smem) + RBM * LS_STRIDE;   // [8 warps][E]
+        {
+            using namespace router_detail;
+            const int fw = warp;
+            const uint32_t ls0 = smem_u32(smem);
+            float pacc[FNV];
+#pragma unroll
+            for (int i = 0; i < FNV; i++) pacc[i] = 0.f;
+            for (int t = t_beg + fw; t < t_end; t += kFinishWarps) {
+                const int64_t tok = (int64_t)m0 + t;
+                if (tok >= N) break;
+                float v[FNV];
+#pragma unroll
+                for (int i = 0; i < FNV; i++) {
+                    const int e = lane + 32 * i;
+                    v[i] = e < E ? ld_cluster_f32(mapa_shared(ls0, (uint32_t)(e / REN)) +
+                                                  (uint32_t)((t * LS_STRIDE + e % REN) * 4))
+                                 : 0.f;
+                }
+                finish_token<FNV>(v, fin.b_r, fin.bias_mode, E, fin.k, fin.renorm, tok, fin.idx,
+                                  fin.w, fin.gap, fin.lse, fin.probs, pacc);
+            }
+            // this CTA's column sums of the probabilities, added over its warps in warp order
+#pragma unroll
+            for (int i = 0; i < FNV; i++)
+                if (lane + 32 * i < E) ptab[fw * E + lane + 32 * i] = pacc[i];
+            asm volatile("bar.sync 1, %0;" ::"r"(kFinishWarps * 32) : "memory");
+            const int64_t prow = (int64_t)blockIdx.x * cy + blockIdx.y;
+            for (int e = threadIdx.x; e < E; e += kFinishWarps * 32) {
+                float sacc = 0.f;
+                for (int w2 = 0; w2 < kFinishWarps; w2++) sacc += ptab[w2 * E + e];
+                fin.p_part[prow * E + e] = sacc;
+            }
+        }
+        cluster_sync_all();   // no CTA leaves while a peer may still read its logits
     }
     if (threadIdx.x == 0 && *abort_flag && err) atomicOr(err, MOE_DEVERR_TIMEOUT);
 }
@@ -291,26 +373,75 @@ size_t router_tc_logits_floats(int64_t N, int d, int E) {
     return (size_t)N * E * (router_tc_split(N, d, E) > 1 ? 1 + nslices : 1);
 }
 
-cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const float* W_r, int E,
-                             __nv_bfloat16* w3, float* logits, int32_t* err, cudaStream_t s) {
-    if (N <= 0) return cudaSuccess;
+cudaError_t tc_router_split(const float* W_r, int E, int d, __nv_bfloat16* w3, cudaStream_t s) {
     const int64_t n = (int64_t)E * d;
     int blocks = (int)((n + 255) / 256);
     if (blocks > 148 * 8) blocks = 148 * 8;
     split3_kernel<<<blocks, 256, 0, s>>>(W_r, n, w3);
-    cudaError_t e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+bool router_tc_fused(int64_t N, int d, int E) {
+    return router_tc_split(N, d, E) == 1 && E > 3 * REN && E <= 8 * REN;
+}
+
+template <int FNV>
+cudaError_t launch_fused(const CUtensorMap& mx, const CUtensorMap& mw, int64_t N, int d, int E,
+                         int nslices, int32_t* err, const RouterFinish& fin, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<FNV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM);
     if (e != cudaSuccess) return e;
+    const int cy = (E + REN - 1) / REN;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + RBM - 1) / RBM), (unsigned)cy, 1);
+    cfg.blockDim = dim3(RTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = RSMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = (unsigned)cy;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_tc_kernel<FNV>, mx, mw, N, d, E, nslices,
+                              (float*)nullptr, (float*)nullptr, err, fin);
+}
+
+cudaError_t tc_router_fused(const __nv_bfloat16* x, int64_t N, int d, const __nv_bfloat16* w3,
+                            int E, const float* b_r, int bias_mode, int k, int renorm,
+                            int32_t* idx, float* w, float* gap, float* lse, float* probs,
+                            float* p_part, int32_t* err, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
     CUtensorMap mx, mw;
     if (!make_map(&mx, x, N, d, RBM) || !make_map(&mw, w3, 3 * (int64_t)E, d, REN))
         return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM);
+    const int nslices = ((d + RBK - 1) / RBK + SLICE_KB - 1) / SLICE_KB;
+    const RouterFinish fin{b_r, bias_mode, k, renorm, idx, w, gap, lse, probs, p_part};
+    if (E <= 64) return launch_fused<2>(mx, mw, N, d, E, nslices, err, fin, s);
+    if (E <= 128) return launch_fused<4>(mx, mw, N, d, E, nslices, err, fin, s);
+    if (E <= 256) return launch_fused<8>(mx, mw, N, d, E, nslices, err, fin, s);
+    return launch_fused<16>(mx, mw, N, d, E, nslices, err, fin, s);
+}
+
+int router_tc_part_rows(int64_t N, int E) { return (int)((N + RBM - 1) / RBM) * ((E + REN - 1) / REN); }
+
+cudaError_t tc_router_logits(const __nv_bfloat16* x, int64_t N, int d, const __nv_bfloat16* w3,
+                             int E, float* logits, int32_t* err, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
+    cudaError_t e;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, N, d, RBM) || !make_map(&mw, w3, 3 * (int64_t)E, d, REN))
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(router_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM);
     if (e != cudaSuccess) return e;
     const int nslices = ((d + RBK - 1) / RBK + SLICE_KB - 1) / SLICE_KB;
     const int z = router_tc_split(N, d, E);
     const int spc = (nslices + z - 1) / z;
     float* slices = z > 1 ? logits + N * E : nullptr;   // the region is sized by router_tc_logits_floats
     dim3 grid((unsigned)((N + RBM - 1) / RBM), (unsigned)((E + REN - 1) / REN), (unsigned)z);
-    router_tc_kernel<<<grid, RTHREADS, RSMEM, s>>>(mx, mw, N, d, E, spc, logits, slices, err);
+    router_tc_kernel<0><<<grid, RTHREADS, RSMEM, s>>>(mx, mw, N, d, E, spc, logits, slices, err,
+                                                      RouterFinish{});
     e = cudaGetLastError();
     if (e != cudaSuccess || z == 1) return e;
     const int64_t NE = N * E;

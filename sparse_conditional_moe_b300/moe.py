@@ -27,7 +27,8 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_grouped_rows", "moe_
            "moe_forward_traced", "moe_forward_buffers", "moe_stats", "moe_device_error",
            "moe_selftest_wait_timeout", "moe_status_string", "moe_status_str", "moe_quantize_w4",
            "moe_grouped_ffn_w4a16", "moe_forward_w4a16", "moe_router_stats",
-           "moe_selftest_gemm", "moe_backward_workspace_size", "moe_backward")
+           "moe_selftest_gemm", "moe_backward_workspace_size", "moe_backward",
+           "moe_router_prepare")
 MOE_W4_GROUP = 128
 
 
@@ -87,6 +88,7 @@ def lib():
         sig = {
             "moe_workspace_size": [C, ctypes.POINTER(SZ)],
             "moe_workspace_init": [C, P, SZ, P],
+            "moe_router_prepare": [C, P, P, SZ, P],
             "moe_route": [C, P, P, P, P, P, P, P, P, SZ, P],
             "moe_permute": [C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "moe_permute_noalloc": [C, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
@@ -166,6 +168,14 @@ def moe_grouped_rows(cfg: MoeCfg) -> int:
     if r < 0:
         raise MoeError(1, "moe_grouped_rows")
     return r
+
+
+def moe_router_prepare(cfg: MoeCfg, W_r: torch.Tensor, ws: torch.Tensor, stream=None):
+    """Write the router weight's exact bf16 split into the workspace once (see include/moe.h);
+    later calls with this workspace and this W_r tensor skip the split.  Call again after
+    changing W_r in place."""
+    _check(lib().moe_router_prepare(ctypes.byref(cfg), _p(W_r), _p(ws), ws.numel(), _s(stream)),
+           "moe_router_prepare")
 
 
 def moe_workspace_init(cfg: MoeCfg, ws: torch.Tensor, stream=None):
@@ -409,6 +419,12 @@ class MoELayer:
         self.ws = workspace(cfg, self.device)
         act = torch.bfloat16 if cfg.act_dtype == MOE_BF16 else torch.float32
         self.out = torch.empty((cfg.N, cfg.d), dtype=act, device=self.device)
+        self.prepare_router()
+
+    def prepare_router(self, stream=None):
+        """(Re)write the router weight's split into the workspace: call after changing
+        weights["W_r"] in place."""
+        moe_router_prepare(self.cfg, self.w["W_r"], self.ws, stream)
 
     def forward(self, x: torch.Tensor, stream=None, events=None,
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
