@@ -159,7 +159,8 @@ MOE_API moe_status moe_permute(const moe_cfg *cfg, const int32_t *idx, const flo
  *     larger calls return MOE_ERR_WORKSPACE.  The call allocates nothing.
  *   - err [1] int32, nullable, device: MOE_DEVERR_* bits are OR-ed into it (caller clears it).
  *   - all calls share the array: calls that overlap on the GPU race.  The first call on each
- *     device looks up the array's address; make it before any stream capture.
+ *     device looks up the array's address and keeps it; make it before any stream capture.  A
+ *     device reset (cudaDeviceReset) after that first call is not supported.
  */
 MOE_API moe_status moe_permute_noalloc(const moe_cfg *cfg, const int32_t *idx, const float *w,
                                        const void *x, int32_t *counts, int32_t *offsets,

@@ -17,8 +17,11 @@ int64_t router_part_rows(int64_t N);
 
 // ------------------------------------------------------------------ permute tiling
 
+// A grouping block covers 2048 consecutive slots.  A full block gives each of its 8 warps 256
+// (8 steps of 32); a short last block spreads its slots evenly over the warps (each warp a
+// contiguous run, in warp order), so kPermSlotsPerWarp is the most a warp ever handles.
 constexpr int kPermThreads = 256;                    // 8 warps
-constexpr int kPermSlotsPerWarp = 256;               // 8 steps of 32 slots
+constexpr int kPermSlotsPerWarp = 256;
 constexpr int kPermSlotsPerBlock = kPermSlotsPerWarp * (kPermThreads / 32);
 inline int perm_blocks(int64_t slots) {
     return (int)((slots + kPermSlotsPerBlock - 1) / kPermSlotsPerBlock);

@@ -16,7 +16,9 @@
 //     it has to start at zero: each call writes every entry it later reads.  Calls whose work
 //     overlaps on the GPU (for instance on two streams without ordering) race on the array.
 //   - The first call on each device looks up the array's device address (with that device
-//     current); make that first call before any stream capture.
+//     current) and keeps it for the life of the process; make that first call before any stream
+//     capture.  A device reset (cudaDeviceReset) after that first call is not supported: the
+//     module is loaded again at another address while the kept one goes stale.
 #include <mutex>
 
 #include "moe_internal.cuh"

@@ -2,9 +2,10 @@
 
 The GPU runs the expert products on bf16 operands (dout, dh, dG, dU and w h rounded to bf16,
 fp32 accumulation) where the oracle stays in fp64 with only h rounded (the forward's rounding
-point); each rounding adds ~2^-9 relative error with random sign, so the bar is a relative
-Frobenius error <= 2e-2 per gradient tensor (per touched expert for the expert matrices),
-untouched experts exactly 0, and the selection-only bias's gradient exactly 0.  The routing must
+point); each rounding adds ~2^-9 relative error with random sign, so the bar is a relative L2
+error <= 2e-2 per row: every token's dx, every row of dW_r and of every touched expert's
+matrices (a row that nearly cancels is held to 2e-2 of 5 % of the rms row norm instead of its
+own), untouched experts exactly 0, and the selection-only bias's gradient exactly 0.  The routing must
 be the oracle's bit for bit on these seeds (no near ties), else the gradients are not comparable.
 """
 import numpy as np
@@ -39,6 +40,19 @@ def rel(a, b):
     return np.linalg.norm(a - b) / nb if nb > 0 else np.linalg.norm(a)
 
 
+def rows_close(got, ref, what, floor=0.05):
+    """Row by row: ||got_r - ref_r|| <= REL * max(||ref_r||, floor * rms row norm).  The floor
+    keeps rows that nearly cancel (their bf16 rounding error scales with the terms, not with
+    the small sum) from failing on their own magnitude; every other row is held to REL."""
+    got = np.asarray(got, np.float64).reshape(got.shape[0], -1)
+    ref = np.asarray(ref, np.float64).reshape(ref.shape[0], -1)
+    nref = np.linalg.norm(ref, axis=1)
+    scale = np.maximum(nref, floor * np.sqrt(np.mean(nref ** 2)))
+    err = np.linalg.norm(got - ref, axis=1)
+    bad = np.nonzero(err > REL * scale)[0]
+    assert bad.size == 0, (what, bad[:8], (err[bad] / np.maximum(scale[bad], 1e-300))[:8])
+
+
 @pytest.mark.parametrize("case", LAYERS, ids=lambda c: c[0].name)
 def test_backward_matches_oracle(case):
     spec, aux, zc = case
@@ -57,8 +71,8 @@ def test_backward_matches_oracle(case):
     ref = oracle.backward(L, spec.k, oracle.BF16, dout.double().numpy(), cf=spec.capacity_factor,
                           bias_mode=bm, aux_coef=aux, z_coef=zc)
     got = {k: v.cpu().numpy() for k, v in g.items()}
-    assert rel(got["dx"], ref["dx"]) <= REL, rel(got["dx"], ref["dx"])
-    assert rel(got["dW_r"], ref["dW_r"]) <= REL, rel(got["dW_r"], ref["dW_r"])
+    rows_close(got["dx"], ref["dx"], "dx")                 # every token
+    rows_close(got["dW_r"], ref["dW_r"], "dW_r")           # every expert's router row
     if bm == 1:
         assert rel(got["db"], ref["db"]) <= REL
     else:
@@ -67,12 +81,13 @@ def test_backward_matches_oracle(case):
     for e in range(spec.E):
         for name in ("dW_gate", "dW_up", "dW_down"):
             if e in touched and np.any(ref[name][e] != 0):
-                assert rel(got[name][e], ref[name][e]) <= REL, (name, e, rel(got[name][e], ref[name][e]))
+                rows_close(got[name][e], ref[name][e], (name, e))   # every row of the matrix
             elif e not in touched:
                 assert np.all(got[name][e] == 0), (name, e)
     if spec.n_shared:
         for name in ("dWs_gate", "dWs_up", "dWs_down"):
-            assert rel(got[name], ref[name]) <= REL, (name, rel(got[name], ref[name]))
+            for s_ in range(spec.n_shared):
+                rows_close(got[name][s_], ref[name][s_], (name, s_))
 
 
 def test_backward_is_deterministic():

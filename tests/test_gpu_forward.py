@@ -3,8 +3,10 @@
 Small layers (the oracle finishes in seconds) are compared on every token: routing bit-exact
 (near-ties excluded), counts / offsets / permutation / positions bit-exact, outputs within the
 stated tolerance.  The five workload layers are compared at their full sizes in the launch
-configuration the benchmark uses: routing and grouping on every token, outputs on a seeded
-sample of tokens the oracle computes one by one.
+configuration the benchmark uses: routing and grouping on every token, outputs on the tokens the
+oracle computes one by one -- every token of the small-batch layers, and on the prefill-sized
+layers a token on every tile of the grouped GEMMs (each expert's first grouped row and the last
+row of each of its 256-row chunks) plus a seeded sample.
 """
 import numpy as np
 import pytest
@@ -152,6 +154,37 @@ def test_stats_match_oracle():
 
 FULL = [moe_synth.TINY, moe_synth.MIXTRAL, moe_synth.DSV3_PREFILL, moe_synth.DSV3_DECODE,
         moe_synth.QWEN3_SKEWED]
+CHUNK = 256   # token rows per tile of the CTA-pair grouped GEMMs
+
+
+def chunk_cover_tokens(spec, idx_o, cap):
+    """Tokens whose grouped rows cover every tile of the grouped GEMMs: for every expert the
+    first grouped row, and the last row of each of its chunks (a group of n kept rows is cut into
+    ceil(n / 256) chunks split evenly, the MMA's N rounded up to 16: the last row sits next to
+    the chunk's padding).  Returns sorted token indices."""
+    ref = oracle.permute(idx_o, spec.E, cap)
+    pos = ref["pos"].reshape(-1)
+    kept, koff = ref["kept"], ref["kept_offsets"]
+    row_slot = np.full(int(koff[-1]), -1, np.int64)
+    live = np.nonzero(pos >= 0)[0]
+    row_slot[pos[live]] = live
+    rows = []
+    for e in range(spec.E):
+        n = int(kept[e])
+        if n == 0:
+            continue
+        base = int(koff[e])
+        nch = -(-n // CHUNK)
+        b, rem = divmod(n, nch)
+        start = 0
+        rows.append(base)
+        for c in range(nch):
+            rc = b + (1 if c < rem else 0)
+            rows.append(base + start + rc - 1)
+            start += rc
+    slots = row_slot[np.array(rows, np.int64)]
+    assert np.all(slots >= 0)
+    return np.unique(slots // spec.k)
 
 
 @pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
@@ -172,8 +205,11 @@ def test_forward_full_size_workloads(spec):
     keep_o = oracle.keep_naive(idx_o, spec.E, cap)
     if spec.capacity_factor > 0:
         assert keep_o.min() == 0       # the skewed layer really overflows some experts
-    n_sample = {"tiny_fp32": 64, "deepseek_v3_decode_bf16": 24}.get(spec.name, 12)
-    tok = moe_synth.sample_tokens(spec.N, n_sample, seed=1).numpy()
+    if spec.N <= 64:                   # the tiny and decode layers: every token
+        tok = np.arange(spec.N)
+    else:                              # a token on every tile of the grouped GEMMs + a sample
+        tok = np.union1d(chunk_cover_tokens(spec, idx_o, cap),
+                         moe_synth.sample_tokens(spec.N, 12, seed=1).numpy())
     tok = tok[~excl[tok]] if differs.size else tok
     if spec.capacity_factor > 0:       # include tokens that lost assignments
         lost = np.nonzero(keep_o.sum(1) < spec.k)[0]

@@ -57,6 +57,8 @@ def _permute(N, k, E, idx, cf=0.0, d=64, dtype=moe.MOE_BF16, seed=0):
     (2000, 8, 128, 1.25, 1.2),         # capacity with a skewed router
     (700, 2, 8, 0.3, 1.0),             # most assignments dropped
     (5, 3, 3, 0.0, 0.0),               # k = E
+    (1025, 2, 16, 0.0, 0.0),           # last block of 2 slots: most of its warps get none
+    (4101, 2, 64, 1.0, 1.0),           # 4 full blocks and a 10-slot one, with capacity
 ])
 def test_permute_matches_oracle(N, k, E, cf, skew):
     idx = _random_idx(N * 7 + E, N, k, E, skew)

@@ -157,3 +157,27 @@ def test_prepared_router_split_is_never_stale():
         idx, w, gap = route(W)
         idx_o, w_o, probs_o, gap_o = want[name]
         check_routing(idx, w, gap, idx_o, w_o, probs_o, gap_o)
+
+
+@pytest.mark.parametrize("label,N,d,E,k,dt", [
+    ("gemv (E <= 32)", 4096, 4096, 8, 2, "bf16"),
+    ("tensor cores, d split (N <= 1024)", 1024, 7168, 256, 8, "bf16"),
+    ("tensor cores + top-k kernel", 4096, 2048, 128, 8, "bf16"),
+    ("tensor cores, fused", 4096, 7168, 256, 8, "bf16"),
+    ("fp32 tiled", 2048, 1024, 128, 8, "f32"),
+])
+def test_weight_error_per_router_path(label, N, d, E, k, dt):
+    """Measured max |w - w_oracle| and max |gap - gap_oracle| of each router path on a large
+    batch (printed for the record; held to the stated 2e-6)."""
+    spec = moe_synth.LayerSpec("rw", N=N, d=d, d_ff=64, E=E, k=k, dtype=dt)
+    L = moe_synth.make_layer(spec, seed=29, x_only=True)
+    idx, w, P, gap = _route(spec, L)
+    idx_o, w_o, probs_o, gap_o = oracle.route(L["x"], L["W_r"], None, k, dtype_code(spec))
+    excl, differs = check_routing(idx, w, gap, idx_o, w_o, probs_o, gap_o)
+    same = np.all(idx == idx_o, axis=1) & ~excl
+    dw = np.abs(w[same].astype(np.float64) - w_o[same]).max()
+    fin = np.isfinite(gap_o)
+    dg = np.abs(gap[fin].astype(np.float64) - gap_o[fin]).max()
+    print(f"\nrouter weight error [{label}] N={N} d={d} E={E} k={k}: max|dw| = {dw:.3e}, "
+          f"max|dgap| = {dg:.3e}, tokens compared {int(same.sum())}")
+    assert dw <= 2e-6 and dg <= 2e-6

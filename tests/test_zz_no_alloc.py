@@ -2,14 +2,16 @@
 workspace (their device memory is owned by another allocator, or their interface has no place
 for one).  Its per-block tables live in a fixed device array inside the library, shared by all
 calls.  These tests call it through the C ABI and require its outputs to be identical to
-moe_permute's (integer and copy outputs: bit-exact) on two different calls in a row, so
-whatever the first call left in the shared array cannot leak into the second."""
+moe_permute's and to the oracle's grouping (integer and copy outputs: bit-exact) on two
+different calls in a row, so whatever the first call left in the shared array cannot leak into
+the second."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from sparse_conditional_moe_b300 import moe
 
 pytestmark = pytest.mark.gpu
@@ -53,7 +55,24 @@ def _both(N, k, E, d, cf, skew, seed):
                             got["row_weight"], got["x_perm"], err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and moe.moe_device_error(ws) == 0
+    _oracle_check(N, k, E, cf, idx.cpu().numpy(), w.cpu().numpy(), x.cpu(), got)
     return ref, got
+
+
+def _oracle_check(N, k, E, cf, idx, w, x, got):
+    """The oracle's grouping (counting sort, keep the first C of each expert in slot order) and
+    the rows it implies: row r holds slot f, token f // k, weight w[f], activations x[f // k]."""
+    ref = oracle.permute(idx, E, oracle.capacity(N, k, E, cf))
+    for key in ("counts", "offsets", "kept", "kept_offsets", "perm", "pos"):
+        assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+    M = int(ref["kept_offsets"][-1])
+    pos = ref["pos"].reshape(-1)
+    live = np.nonzero(pos >= 0)[0]
+    row_slot = np.empty(M, np.int64)
+    row_slot[pos[live]] = live
+    assert np.array_equal(got["row_token"][:M].cpu().numpy(), row_slot // k)
+    assert np.array_equal(got["row_weight"][:M].cpu().numpy(), w.reshape(-1)[row_slot])
+    assert torch.equal(got["x_perm"][:M].cpu(), x[torch.from_numpy(row_slot // k)])
 
 
 def test_noalloc_matches_moe_permute_on_two_calls_in_a_row():
