@@ -204,10 +204,12 @@ MOE_API moe_status moe_combine(const moe_cfg *cfg, const void *y_perm, const int
  * moe_forward_buffers).  Arguments as in the step calls; out [N,d] act dtype.
  * For a bf16 batch of at most 128 tokens with shared experts, the shared experts run on a stream
  * owned by the library, forked from `stream` when the call starts (after all work already on
- * `stream`) and joined back before the combine: the call stays ordered on `stream`, including
- * under stream capture.  Larger batches use `stream` only.  The same holds for
- * moe_forward_traced and moe_forward_w4a16; there the "shared" phase then measures the wait
- * for the join.
+ * `stream`) and joined back before the combine (also when the call returns an error after the
+ * fork): the call stays ordered on `stream`, including under stream capture.  That stream
+ * belongs to the calling host thread (one per device and thread, kept until exit), so calls
+ * from different threads, capturing or not, never share it.  Larger batches use `stream`
+ * only.  The same holds for moe_forward_traced and moe_forward_w4a16; there the "shared" phase
+ * then measures the wait for the join.
  */
 MOE_API moe_status moe_forward(const moe_cfg *cfg, const void *x, const float *W_r, const float *b_r,
                        const void *W_gate, const void *W_up, const void *W_down,

@@ -119,12 +119,14 @@ combine_kernel(const T* __restrict__ y, const int32_t* __restrict__ pos, const T
     }
 }
 
-// mtile_off[e] = sum_{e' < e} ceil(kept[e'] / bm), one block, E <= 1024.
+// mtile_off[i] = sum_{i' < i} ceil(kept[g(i')] / bm), one block, E <= 1024, where g is the
+// identity or, with zigzag, the order 0, E-1, 1, E-2, ... (zigzag_group).
 __global__ void __launch_bounds__(1024)
-plan_kernel(const int32_t* __restrict__ kept, int E, int bm, int32_t* __restrict__ mtile_off) {
+plan_kernel(const int32_t* __restrict__ kept, int E, int bm, int zigzag,
+            int32_t* __restrict__ mtile_off) {
     __shared__ int tmp[33];
     const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-    const int v = e < E ? (kept[e] + bm - 1) / bm : 0;
+    const int v = e < E ? (kept[zigzag ? zigzag_group(e, E) : e] + bm - 1) / bm : 0;
     int inc = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -283,8 +285,8 @@ cudaError_t launch_combine(const moe_cfg& c, const void* y_perm, const int32_t* 
 }
 
 cudaError_t launch_plan_mtiles(const int32_t* kept, int E, int bm, int32_t* mtile_off,
-                               cudaStream_t s) {
-    plan_kernel<<<1, 1024, 0, s>>>(kept, E, bm, mtile_off);
+                               cudaStream_t s, bool zigzag) {
+    plan_kernel<<<1, 1024, 0, s>>>(kept, E, bm, zigzag ? 1 : 0, mtile_off);
     return cudaGetLastError();
 }
 

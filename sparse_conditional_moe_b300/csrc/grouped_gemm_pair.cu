@@ -37,6 +37,8 @@
 // gate warp finishes silu(g) * u and the store.
 // Tiles run group-major, then by weight tile, with the chunks of a group innermost (in blocks of
 // 16 chunks), so the pairs working at the same time share weight tiles and token chunks in L2.
+// Routed groups run in the order 0, E-1, 1, E-2, ... so that, under a router that loads one end
+// of the expert range (the Zipf-biased layer), tiles of heavy and light experts run side by side.
 // A decode-sized variant (at most 64 rows per group) keeps 32-row token slots and 9 stages, so
 // more weight bytes are in flight per SM where the GEMMs stream weights.
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises an abort flag, the other
@@ -83,7 +85,9 @@ struct PairParams {
     int G;
     const int32_t* rows;        // [G] device, or nullptr for uniform groups
     const int32_t* row_off;     // [G] device (token row of the group's first row)
-    const int32_t* chunk_off;   // [G+1] prefix of the groups' 256-row chunks (non-uniform)
+    const int32_t* chunk_off;   // [G+1] prefix of the groups' 256-row chunks (non-uniform),
+                                // over the groups in zigzag_group order when zigzag is set
+    int zigzag;
     int uniform_rows;
     int64_t a_stride, c_stride;
     int K;             // reduction length
@@ -130,11 +134,11 @@ __device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile) {
             if (p.chunk_off[mid] * p.n_wt <= tile) lo = mid;
             else hi = mid;
         }
-        t.g = lo;
+        t.g = p.zigzag ? zigzag_group(lo, p.G) : lo;
         nch = p.chunk_off[lo + 1] - p.chunk_off[lo];
         local = tile - p.chunk_off[lo] * p.n_wt;
-        n = p.rows[lo];
-        a0 = c0 = p.row_off[lo];
+        n = p.rows[t.g];
+        a0 = c0 = p.row_off[t.g];
     }
     raster_tile(local, nch, p.n_wt, t.c, t.w);
     // the group's rows split evenly over its chunks: the first n % nch chunks get one more
@@ -483,6 +487,7 @@ PairParams base_params(const GroupGeom& g) {
     p.rows = g.rows;
     p.row_off = g.row_off;
     p.chunk_off = g.mtile_off;
+    p.zigzag = g.zigzag ? 1 : 0;
     p.uniform_rows = g.uniform_rows;
     p.a_stride = g.a_stride;
     p.c_stride = g.c_stride;

@@ -180,7 +180,8 @@ moe_status do_grouped_ffn(const moe_cfg* c, const void* x_perm, const int32_t* k
     g.mtile_off = mtile;
     g.max_rows = R;
     const int bm = pair_gemm ? pair_chunk_rows() : bf16 ? kTcBlockRows : simt_block_rows();
-    MOE_CUDA(launch_plan_mtiles(kept, c->E, bm, mtile, s));
+    g.zigzag = pair_gemm;
+    MOE_CUDA(launch_plan_mtiles(kept, c->E, bm, mtile, s, g.zigzag));
     void* h = at<void>(ws, L.h_perm);
     if (pair_gemm) {
         MOE_CUDA(pair_gateup(g, (const __nv_bfloat16*)x_perm, R, c->d, (const __nv_bfloat16*)Wg,
@@ -292,6 +293,10 @@ void forget_prepared(const void* ws) {
 // most SMs idle; they depend only on x, so they are forked onto a library-owned stream at the
 // start of the forward and joined before the combine, overlapping the router, the permutation
 // and the routed experts.  Larger batches keep them in line (their GEMMs fill the GPU).
+// The side stream belongs to the calling thread (one per device and host thread, created on its
+// first decode-sized forward and kept until the process exits), so forwards from different
+// threads never meet on it: neither do they serialise there, nor does one thread's stream
+// capture pull in another thread's shared-expert work.
 constexpr int64_t kSideStreamMaxTokens = 128;
 
 bool fork_shared(const moe_cfg& c) {
@@ -299,11 +304,9 @@ bool fork_shared(const moe_cfg& c) {
 }
 
 cudaStream_t side_stream() {
-    static std::mutex mu;
-    static cudaStream_t streams[64] = {};
+    thread_local cudaStream_t streams[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
     if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
         streams[dev] = nullptr;
     return streams[dev];
@@ -329,6 +332,28 @@ moe_status fork_shared_end(cudaStream_t s, cudaStream_t side, cudaEvent_t join) 
     MOE_CUDA(e);
     return MOE_OK;
 }
+
+// Joins a forked side stream back into s when it goes out of scope unless join() already did:
+// an error return between the fork and the join still leaves no unjoined work behind (which
+// under stream capture would turn the caller's error into cudaErrorStreamCaptureUnjoined).
+struct ForkJoin {
+    cudaStream_t s = nullptr, side = nullptr;
+    cudaEvent_t ev = nullptr;
+    bool open = false;
+    moe_status begin(cudaStream_t s_, cudaStream_t side_) {
+        s = s_;
+        side = side_;
+        MOE_TRY(fork_shared_begin(s, side, &ev));
+        open = true;
+        return MOE_OK;
+    }
+    moe_status join() {
+        if (!open) return MOE_OK;
+        open = false;
+        return fork_shared_end(s, side, ev);
+    }
+    ~ForkJoin() { (void)join(); }
+};
 
 // ------------------------------------------------------------------ W4A16 pieces
 
@@ -593,9 +618,9 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     const bool prepared = split_prepared(*cfg, W_r, ws);
     if (!prepared) forget_prepared(ws);
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
-    cudaEvent_t join = nullptr;
+    ForkJoin fj;
     if (side) {
-        MOE_TRY(fork_shared_begin(s, side, &join));
+        MOE_TRY(fj.begin(s, side));
         MOE_TRY(do_shared(cfg, x, Ws_gate, Ws_up, Ws_down, ws, side));
     }
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
@@ -615,7 +640,7 @@ moe_status moe_forward_traced(const moe_cfg* cfg, const void* x, const float* W_
     MOE_TRY(do_grouped_ffn(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                            at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), W_gate,
                            W_up, W_down, at<void>(ws, L.y_perm), ws, s, ev));
-    if (side) MOE_TRY(fork_shared_end(s, side, join));
+    if (side) MOE_TRY(fj.join());
     MOE_TRY(do_shared_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, Ws_gate,
                                   Ws_up, Ws_down, out, ws, s, ev, side != nullptr));
     return MOE_OK;
@@ -683,9 +708,9 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     const bool prepared = split_prepared(*cfg, W_r, ws);
     if (!prepared) forget_prepared(ws);
     cudaStream_t side = fork_shared(*cfg) ? side_stream() : nullptr;
-    cudaEvent_t join = nullptr;
+    ForkJoin fj;
     if (side) {
-        MOE_TRY(fork_shared_begin(s, side, &join));
+        MOE_TRY(fj.begin(s, side));
         MOE_TRY(do_shared_w4(cfg, x, *W, ws, side));
     }
     MOE_CUDA(launch_router(*cfg, x, W_r, b_r, at<int32_t>(ws, L.idx), at<float>(ws, L.w),
@@ -705,7 +730,7 @@ moe_status moe_forward_w4a16(const moe_cfg* cfg, const void* x, const float* W_r
     MOE_TRY(do_grouped_ffn_w4(cfg, at<void>(ws, L.x_perm), at<int32_t>(ws, L.kept),
                               at<int32_t>(ws, L.kept_offsets), at<float>(ws, L.row_weight), *W,
                               at<void>(ws, L.y_perm), ws, s, ev));
-    if (side) MOE_TRY(fork_shared_end(s, side, join));
+    if (side) MOE_TRY(fj.join());
     MOE_TRY(do_shared_w4_and_combine(cfg, at<void>(ws, L.y_perm), at<int32_t>(ws, L.pos), x, *W,
                                      out, ws, s, ev, side != nullptr));
     return MOE_OK;

@@ -91,6 +91,7 @@ struct GroupGeom {
     const int32_t* rows;       // [G] device, or nullptr for uniform rows
     const int32_t* row_off;    // [G] device (A and C row offsets), or nullptr for uniform
     const int32_t* mtile_off;  // [G+1] device m-tile prefix (non-uniform)
+    bool zigzag;               // mtile_off runs over the groups in zigzag_group order
     int uniform_rows;          // rows per group when rows == nullptr
     int64_t a_stride;          // uniform: A row offset of group g = g * a_stride
     int64_t c_stride;          // uniform: C row offset of group g = g * c_stride
@@ -98,9 +99,13 @@ struct GroupGeom {
 };
 
 // m-tile prefix over groups for the routed experts (from kept); bm = the GEMM's tile height.
+// zigzag: the prefix runs over the groups in the order 0, E-1, 1, E-2, ... (zigzag_group), which
+// the CTA-pair GEMMs use so that the tiles of heavy and light groups run side by side when a
+// skewed router puts the heavy groups at one end.
 constexpr int kTcBlockRows = 128;
+__host__ __device__ inline int zigzag_group(int i, int E) { return (i & 1) ? E - 1 - (i >> 1) : (i >> 1); }
 cudaError_t launch_plan_mtiles(const int32_t* kept, int E, int bm, int32_t* mtile_off,
-                               cudaStream_t s);
+                               cudaStream_t s, bool zigzag = false);
 
 // bf16 tcgen05 grouped SwiGLU (gate|up) GEMM: H = silu(A Wg^T) * (A Wu^T)
 cudaError_t tc_gateup(const GroupGeom& g, const __nv_bfloat16* A, int64_t a_rows, int K,
