@@ -522,35 +522,53 @@ def measure(spec, args, peaks, torch, dist, world, rank, local, headline: bool):
 
 
 def phase_rooflines(spec, act_b, w_b, kept_rows, touched, ph_ms, peaks):
-    """Achieved rate of every phase against its own bound (algorithmic work only): the GEMM
-    phases in TFLOP/s against the burst bf16 peak, the data-movement phases in GB/s against HBM.
-    w_b: bytes per expert weight (the activation size, or 0.53125 for W4A16)."""
+    """Achieved rate of every phase against its own bound (algorithmic work only).  A GEMM phase
+    has both a tensor bound (flops / burst bf16 peak) and an HBM bound (weights of the touched
+    experts + rows read and written, / HBM bandwidth); the larger ideal time binds, and the phase
+    is reported in that bound's unit, with the other bound's fraction beside it.  The
+    data-movement phases are HBM-bound.  w_b: bytes per expert weight (the activation size, or
+    0.53125 for W4A16)."""
     d, F, E, N, S, Fs = spec.d, spec.d_ff, spec.E, spec.N, spec.n_shared, spec.d_ff_shared
     tf_peak, gb_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
     w_bytes = w_b * d * F
-    work = {
-        # x read + W_r read
-        "route": ("GB/s", N * d * act_b + 4.0 * d * E),
-        # x rows read + grouped rows written (+ indices)
-        "permute": ("GB/s", 2.0 * kept_rows * d * act_b + 16.0 * N * spec.k),
-        "gateup": ("TFLOP/s", accounting.gateup_flops(d, F, kept_rows)),
-        "down": ("TFLOP/s", accounting.down_flops(d, F, kept_rows)),
-        "shared": ("TFLOP/s", 6.0 * d * Fs * N * S),
-        # grouped rows + shared rows read, out written
-        "combine": ("GB/s", (kept_rows + S * N) * d * act_b + N * d * act_b),
+    rows_io = kept_rows * (d + F) * act_b
+    gemm = {   # phase: (flops, bytes)
+        "gateup": (accounting.gateup_flops(d, F, kept_rows), 2.0 * w_bytes * touched + rows_io),
+        "down": (accounting.down_flops(d, F, kept_rows), 1.0 * w_bytes * touched + rows_io),
+        "shared": (6.0 * d * Fs * N * S, 3.0 * w_b * d * Fs * S + 2.0 * N * (d + Fs) * act_b * S),
     }
-    if spec.N <= 1024:   # decode-sized: the GEMMs stream weights, HBM is their bound
-        work["gateup"] = ("GB/s", 2.0 * w_bytes * touched + kept_rows * (d + F) * act_b)
-        work["down"] = ("GB/s", 1.0 * w_bytes * touched + kept_rows * (d + F) * act_b)
-        work["shared"] = ("GB/s", 3.0 * w_b * d * Fs * S + N * (d + Fs) * act_b * 2)
+    moves = {
+        # x read + W_r read
+        "route": N * d * act_b + 4.0 * d * E,
+        # x rows read + grouped rows written (+ indices)
+        "permute": 2.0 * kept_rows * d * act_b + 16.0 * N * spec.k,
+        # grouped rows + shared rows read, out written
+        "combine": (kept_rows + S * N) * d * act_b + N * d * act_b,
+    }
     out = {}
-    for ph, (unit, amount) in work.items():
-        ms = ph_ms.get(ph, 0.0)
-        if ms <= 0 or amount <= 0:
+    for ph, ms in ph_ms.items():
+        if ms <= 0:
             continue
-        rate = amount / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
-        peak = tf_peak if unit == "TFLOP/s" else gb_peak
-        out[ph] = {"ms": ms, "achieved": rate, "unit": unit, "frac": rate / peak}
+        sec = ms / 1e3
+        if ph in gemm:
+            flops, nbytes = gemm[ph]
+            if flops <= 0:
+                continue
+            t_tensor, t_hbm = flops / (tf_peak * 1e12), nbytes / (gb_peak * 1e9)
+            tensor = {"achieved": flops / sec / 1e12, "unit": "TFLOP/s"}
+            tensor["frac"] = tensor["achieved"] / tf_peak
+            hbm = {"achieved": nbytes / sec / 1e9, "unit": "GB/s"}
+            hbm["frac"] = hbm["achieved"] / gb_peak
+            if t_tensor >= t_hbm:
+                out[ph] = {"ms": ms, "bound": "tensor", **tensor, "hbm_frac": hbm["frac"],
+                           "flops": flops, "bytes": nbytes}
+            else:
+                out[ph] = {"ms": ms, "bound": "hbm", **hbm, "tensor_frac": tensor["frac"],
+                           "flops": flops, "bytes": nbytes}
+        elif ph in moves:
+            rate = moves[ph] / sec / 1e9
+            out[ph] = {"ms": ms, "bound": "hbm", "achieved": rate, "unit": "GB/s",
+                       "frac": rate / gb_peak, "bytes": moves[ph]}
     return out
 
 
@@ -579,22 +597,24 @@ def read_traffic(kernel: str, workload: str):
 
 
 def roofline_of(spec, res, peaks, peak_src):
+    """The dominant kernel (the routed gate/up launch) against the bound that binds it."""
     g = res["gateup"]
-    if g["unit"] == "TFLOP/s":
-        return {"kernel": "routed grouped gate/up SwiGLU GEMM (tcgen05, CTA pairs)",
-                "bound": "tensor", "achieved": g["achieved"], "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": g["achieved"] / peaks["bf16_tflops"],
-                "traffic": read_traffic("gateup", spec.name),
-                "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM, best of 10)",
-                "ms_per_launch": g["ms"],
-                "work_per_launch": f"4*d*d_ff*kept_rows = "
-                                   f"{accounting.gateup_flops(spec.d, spec.d_ff, res['layer']['kept_rows']):.4g} flop"}
     kern = ("routed grouped W4A16 gate/up SwiGLU (TMA + mma.sync)" if spec.w4a16
             else "routed grouped gate/up SwiGLU GEMM (tcgen05, CTA pairs)")
-    return {"kernel": kern, "bound": "hbm", "achieved": g["achieved"], "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": g["frac"], "traffic": None if spec.w4a16 else
-            read_traffic("gateup", spec.name),
-            "peak_source": f"{peak_src} HBM copy bandwidth", "ms_per_launch": g["ms"]}
+    traffic = None if spec.w4a16 else read_traffic("gateup", spec.name)
+    common = {"kernel": kern, "achieved": g["achieved"], "unit": g["unit"], "frac": g["frac"],
+              "traffic": traffic, "ms_per_launch": g["ms"],
+              "work_per_launch": {"flop": g["flops"], "bytes": g["bytes"],
+                                  "flop_formula": "4*d*d_ff*kept_rows",
+                                  "bytes_formula": "2*d*d_ff*w_bytes*touched_experts + "
+                                                   "kept_rows*(d + d_ff)*act_bytes"}}
+    if g["bound"] == "tensor":
+        return {"bound": "tensor", "peak": peaks["bf16_tflops"], **common,
+                "hbm_frac": g["hbm_frac"],
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS bf16 GEMM, best of 10)"}
+    return {"bound": "hbm", "peak": peaks["hbm_gbs"], **common, "tensor_frac": g["tensor_frac"],
+            "tensor_peak": peaks["bf16_tflops"],
+            "peak_source": f"{peak_src} HBM copy bandwidth (tensor: bf16 burst)"}
 
 
 # ------------------------------------------------------------------ main

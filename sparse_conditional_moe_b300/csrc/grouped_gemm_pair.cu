@@ -16,15 +16,18 @@
 // at most 15 computed rows per chunk are padding, and every tile moves a full 256-row weight
 // tile per k-block for all of its tokens.  On a pair each CTA stages its own 128 weight rows and
 // half of the chunk's tokens, so an SM pulls at most 32 KB per 64-wide k-block for 128 x 256 x 64
-// multiply-adds (a single-CTA 128 x 256 tile needs 48 KB for the same work), and the ring holds
-// 6 such stages in shared memory.
+// multiply-adds (a single-CTA 128 x 256 tile needs 48 KB for the same work), and 192 KB of
+// shared memory hold 7 weight and 5 token k-blocks.
 //
-// Roles (320 threads per CTA, one CTA per SM, persistent over the pair's tiles):
-//   warp 0      TMA producer in each CTA: its weight rows and its half of the tokens into the
-//               ring; both CTAs' copies complete on the leader CTA's barrier;
+// Roles (352 threads per CTA, one CTA per SM, persistent over the pair's tiles):
+//   warp 0      weight producer in each CTA: its weight rows into the weight ring (TMA); both
+//               CTAs' copies complete on the leader CTA's barrier;
+//   warp 10     token producer in each CTA: its half of the chunk's token rows into the token
+//               ring, likewise;
 //   warp 1      allocates 512 TMEM columns in each CTA (two 256-column accumulators); in the
-//               leader CTA one thread issues the pair's MMAs (M = 256, N = chunk rows rounded
-//               up to 16, K = 16) and frees ring slots in both CTAs with multicast commits;
+//               leader CTA it issues the pair's MMAs (M = 256, N = chunk rows rounded up to 16,
+//               K = 16) from one elected lane and frees ring slots in both CTAs with multicast
+//               commits;
 //   warps 2..9  epilogue in each CTA, two warps per TMEM lane quarter taking alternate 32-token
 //               chunks (short tiles are otherwise bound by the epilogue): tcgen05.ld of its 128
 //               weight rows, silu*mul or scale in fp32, one rounding to bf16, stores through
@@ -39,8 +42,10 @@
 // 16 chunks), so the pairs working at the same time share weight tiles and token chunks in L2.
 // Routed groups run in the order 0, E-1, 1, E-2, ... so that, under a router that loads one end
 // of the expert range (the Zipf-biased layer), tiles of heavy and light experts run side by side.
-// A decode-sized variant (at most 64 rows per group) keeps 32-row token slots and 9 stages, so
-// more weight bytes are in flight per SM where the GEMMs stream weights.
+// The routed GEMMs of the large layers stream every expert's weights from HBM once, and their
+// speed is set by how many bytes each SM keeps in flight: the rings fill 192 KB of shared memory
+// (7 weight + 5 token slots of 16 KB; 10 + 8 in the decode-sized variant with 32-row token slots
+// of 4 KB, used when no group has more than 64 rows).
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises an abort flag, the other
 // roles stop at their next wait, TMEM is freed and the device error word gets
 // MOE_DEVERR_TIMEOUT.
@@ -57,7 +62,8 @@ constexpr int TOK_MAX = 256;               // token rows per tile (the MMA's N)
 constexpr int A_STAGE = WROWS * BK * 2;    // 16 KB
 constexpr uint32_t TMEM_COLS = 2 * TOK_MAX;
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int TOK_WARP = 2 + EPI_WARPS;    // the token producer, after the epilogue warps
+constexpr int NUM_THREADS = 32 * (TOK_WARP + 1);
 // Epilogue shared memory: down = 8 warps x 2 staging buffers x 2 KB; gate/up = 4 exchange buffers
 // (32 lanes x 32 floats, one per warp pair) + 4 gate warps x 2 staging buffers x 2 KB; + flags.
 constexpr int EPI_BYTES = 32768 + 256;
@@ -67,14 +73,22 @@ __host__ __device__ constexpr int tok_box_rows(int b) { return b == 0 ? 8 : 16 *
 
 enum { EPI_SWIGLU = 0, EPI_SCALE = 1 };
 
+// Two rings, each with its own producer warp: weight k-blocks (read from HBM once per weight
+// tile) in A_STAGES slots and token k-blocks (rows of A, re-read by every weight tile of a chunk,
+// mostly L2 hits) in B_STAGES slots.  Measured on the DeepSeek-V3-shaped layer, both kinds of copy
+// take several k-blocks to land under this load: with 128-row token slots 7 + 5 slots beat 8 + 4
+// and 9 + 3 (2 or 3 token slots stall the MMAs) and match 6 + 6; with 32-row slots (decode)
+// 10 + 8 beats 11 + 3 by 11% and matches 9 + 9.
 template <int TOK_SLOT>
 struct PairCfg {
     static constexpr int B_STAGE = TOK_SLOT * BK * 2;
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = TOK_SLOT >= 128 ? 6 : 9;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+    static constexpr int A_STAGES = TOK_SLOT >= 128 ? 7 : 10;
+    static constexpr int B_STAGES = TOK_SLOT >= 128 ? 5 : 8;
+    static constexpr int RING_BYTES = A_STAGES * A_STAGE + B_STAGES * B_STAGE;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + 1024 + 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
     static_assert(B_STAGE % 1024 == 0, "stages stay 1 KB aligned for the 128-byte swizzle");
+    static_assert((2 * A_STAGES + 2 * B_STAGES + 5) * 8 + 8 <= 512, "barriers fit their area");
 };
 
 struct TokMaps {
@@ -179,19 +193,21 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                     const __grid_constant__ TokMaps tmT, const __grid_constant__ CUtensorMap tmC,
                     const PairParams p) {
     using Cfg = PairCfg<TOK_SLOT>;
-    constexpr int STAGES = Cfg::STAGES;
+    constexpr int SA = Cfg::A_STAGES, SB = Cfg::B_STAGES;
     constexpr int B_STAGE = Cfg::B_STAGE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* sA = smem;                              // [STAGES] x 16 KB weight rows
-    uint8_t* sB = smem + STAGES * A_STAGE;           // [STAGES] x B_STAGE token rows
-    uint8_t* sEpi = smem + STAGES * Cfg::STAGE_BYTES;   // epilogue buffers (see EPI_BYTES)
+    uint8_t* sA = smem;                              // [SA] x 16 KB weight rows
+    uint8_t* sB = smem + SA * A_STAGE;               // [SB] x B_STAGE token rows
+    uint8_t* sEpi = smem + Cfg::RING_BYTES;          // epilogue buffers (see EPI_BYTES)
     volatile int* xflag = reinterpret_cast<volatile int*>(sEpi + 32768);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + EPI_BYTES);
-    uint64_t* full = bars;                 // [STAGES] leader: both CTAs' copies landed
-    uint64_t* empty = bars + STAGES;       // [STAGES] both: the pair's MMAs released the slot
-    uint64_t* tfull = bars + 2 * STAGES;   // [2] both: accumulator ready
+    uint64_t* full_a = bars;               // [SA] leader: both CTAs' weight copies landed
+    uint64_t* empty_a = full_a + SA;       // [SA] both: the pair's MMAs released the slot
+    uint64_t* full_b = empty_a + SA;       // [SB] leader: both CTAs' token copies landed
+    uint64_t* empty_b = full_b + SB;       // [SB] both
+    uint64_t* tfull = empty_b + SB;        // [2] both: accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] leader: both CTAs' epilogues drained it
     uint64_t* drain = tempty + 2;          // [1] leader: MMA drain on exit
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -203,9 +219,13 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < SA; s++) {
+            mbar_init(&full_a[s], 1);
+            mbar_init(&empty_a[s], 1);
+        }
+        for (int s = 0; s < SB; s++) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&empty_b[s], 1);
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
@@ -234,61 +254,76 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
     // by every role alike and reported
     constexpr int kMaxBox = TOK_SLOT / 16;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------- TMA producer (both CTAs)
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
-                const PTile t = decode_tile(p, tile);
-                if (t.box > kMaxBox) continue;
-                const int half = t.n_mma >> 1;
-                const int tok_y = (int)(t.a_row0 + (int64_t)rank * half);
-                const uint32_t tx = 2u * (uint32_t)(A_STAGE + tok_box_rows(t.box) * BK * 2);
-                // gate/up: this CTA's 64 hidden units; down: its 128 output rows
-                const int wy = EPI == EPI_SWIGLU ? t.g * p.w_rows + t.w * 128 + (int)rank * 64
-                                                 : t.g * p.w_rows + t.w * 256 + (int)rank * 128;
-                const CUtensorMap* mt = &tmT.m[t.box];
-                for (int kb = 0; kb < nk; kb++) {
-                    if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
-                    const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+    if (warp == 0 || warp == TOK_WARP) {
+        // ------------------------------------ TMA producers (both CTAs): warp 0 the weight ring,
+        // the token warp the token ring.  The whole warp runs the loop and the waits; one elected
+        // lane issues the copies, which complete on the leader CTA's barrier.
+        const bool wts = warp == 0;
+        const int nst = wts ? SA : SB;
+        uint64_t* fullr = wts ? full_a : full_b;
+        uint64_t* emptyr = wts ? empty_a : empty_b;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
+            const PTile t = decode_tile(p, tile);
+            if (t.box > kMaxBox) continue;
+            const int half = t.n_mma >> 1;
+            const int tok_y = (int)(t.a_row0 + (int64_t)rank * half);
+            const uint32_t tx = wts ? 2u * (uint32_t)A_STAGE : 2u * (uint32_t)(tok_box_rows(t.box) * BK * 2);
+            // gate/up: this CTA's 64 hidden units; down: its 128 output rows
+            const int wy = EPI == EPI_SWIGLU ? t.g * p.w_rows + t.w * 128 + (int)rank * 64
+                                             : t.g * p.w_rows + t.w * 256 + (int)rank * 128;
+            const CUtensorMap* mt = &tmT.m[t.box];
+            for (int kb = 0; kb < nk; kb++) {
+                if (!waitw(&emptyr[s], ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    if (leader) mbar_arrive_expect_tx(&fullr[s], tx);
+                    const uint32_t fb = mapa_shared(smem_u32(&fullr[s]), 0);
                     const int kx = kb * BK;
-                    const uint32_t a = smem_u32(sA + s * A_STAGE);
-                    tma_load_2d_pair(a, &tmW0, fb, kx, wy);
-                    if (EPI == EPI_SWIGLU) tma_load_2d_pair(a + A_STAGE / 2, &tmW1, fb, kx, wy);
-                    tma_load_2d_pair(smem_u32(sB + s * B_STAGE), mt, fb, kx, tok_y);
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                    if (wts) {
+                        const uint32_t a = smem_u32(sA + s * A_STAGE);
+                        tma_load_2d_pair(a, &tmW0, fb, kx, wy);
+                        if (EPI == EPI_SWIGLU) tma_load_2d_pair(a + A_STAGE / 2, &tmW1, fb, kx, wy);
+                    } else {
+                        tma_load_2d_pair(smem_u32(sB + s * B_STAGE), mt, fb, kx, tok_y);
                     }
+                }
+                __syncwarp();
+                if (++s == nst) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-            if (!ok) {   // let copies in flight land before the pair can exit
-                const uint64_t t0 = gtimer();
-                while (gtimer() - t0 < 200000ull) {
-                }
+        }
+        if (!ok && lane == 0) {   // let copies in flight land before the pair can exit
+            const uint64_t t0 = gtimer();
+            while (gtimer() - t0 < 200000ull) {
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && leader) {
+        if (leader) {
             // ---------------------------------------------- MMA issuer (leader CTA only)
-            int s = 0;
-            uint32_t ph = 0;
+            // The whole warp runs the loop and the waits; one elected lane issues the MMAs and
+            // the commits (see elect_one).  The ring descriptors advance by adding the slot size
+            // to their address field.
+            int sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0;
             bool ok = true;
             int it = 0;
+            const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+            uint64_t ad = ad0, bd = bd0;
             for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
                 const PTile t = decode_tile(p, tile);
                 if (t.box > kMaxBox) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
-                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+                if (!waitw(&tempty[acc], aph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -296,32 +331,47 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TOK_MAX);
                 const uint32_t idesc = idesc_bf16_f32(2 * WROWS, t.n_mma);
                 for (int kb = 0; kb < nk; kb++) {
-                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
+                    if (!waitw(&full_a[sa], pha, abort_flag) || !waitw(&full_b[sb], phb, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(smem_u32(sA + s * A_STAGE));
-                    const uint64_t bd = sw128_desc(smem_u32(sB + s * B_STAGE));
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; kk++)
-                        umma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
-                                       (kb > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit_pair(&empty[s], 0x3);
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                        for (int kk = 0; kk < BK / 16; kk++)
+                            umma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
+                                           (kb > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit_pair(&empty_a[sa], 0x3);
+                        umma_commit_pair(&empty_b[sb], 0x3);
+                        if (kb == nk - 1) umma_commit_pair(&tfull[acc], 0x3);
+                    }
+                    __syncwarp();
+                    if (++sa == SA) {
+                        sa = 0;
+                        pha ^= 1u;
+                        ad = ad0;
+                    } else {
+                        ad += (uint64_t)(A_STAGE >> 4);
+                    }
+                    if (++sb == SB) {
+                        sb = 0;
+                        phb ^= 1u;
+                        bd = bd0;
+                    } else {
+                        bd += (uint64_t)(B_STAGE >> 4);
                     }
                 }
-                if (ok) umma_commit_pair(&tfull[acc], 0x3);
             }
-            // every MMA issued by this thread completes before TMEM can be released
-            umma_commit_pair(drain, 0x1);
-            wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
+            // every MMA issued by the elected lane completes before TMEM can be released
+            if (elect_one()) {
+                umma_commit_pair(drain, 0x1);
+                wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
+            }
         }
         __syncwarp();
     } else {
         // -------------------------------------------------- epilogue (warps 2..9, both CTAs)
+        static_assert(TOK_WARP == 2 + EPI_WARPS, "warps 2 .. 1 + EPI_WARPS are the epilogue");
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int sub = (warp - 2) >> 2;     // chunks sub, sub + 2, ... of every tile
         const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);

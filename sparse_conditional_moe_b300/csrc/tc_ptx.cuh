@@ -364,6 +364,21 @@ static __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, vol
     }
 }
 
+// elect.sync over the full warp: true on exactly one lane (the same lane while the warp is
+// converged).  Measured on B300: a loop that waits on an mbarrier and then issues tcgen05.mma
+// from one lane chosen by this instruction, with the whole warp running the loop, issues at the
+// tensor rate; the same loop run by one thread (or with a `lane == 0` test) spends ~100 cycles
+// per MMA and holds MMAs of N < 200 well below the tensor rate.
+static __device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Whole warp, convergent; every lane returns the same answer.
 static __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              uint64_t timeout_ns = kWaitTimeoutNs) {
