@@ -113,6 +113,9 @@ constexpr int kRingBytes = kMmaWarps * kStages * kStageBytes;
 constexpr int kXfragBytes = (kChunkK / kW4Group) * 4 * 32 * 16;        // 32 KB
 constexpr int kXsumBytes = (kChunkK / kW4Group) * kTokTile * 4;        // 512 B
 constexpr int kMmaSmem = kRingBytes + kXfragBytes + kXsumBytes + kMmaWarps * kStages * 8 + 16 + 1024;
+static_assert(kChunkK % kW4Group == 0 && (kTokTile * (kChunkK / 8)) % kMmaThreads == 0,
+              "a chunk is whole groups and splits evenly into 16-byte units per thread");
+static_assert(kMmaSmem <= 232448, "shared memory per block");
 static_assert(kStageBytes % 128 == 0 && kBoxBytes % 128 == 0 && kScaleBytes % 128 == 0,
               "TMA destinations must stay 128-byte aligned");
 

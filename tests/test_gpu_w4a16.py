@@ -169,6 +169,49 @@ def test_w4_grouped_ffn_step_rows_against_oracle():
     compare_rows(_gpu_out(y[torch.from_numpy(rows).cuda()]), np.stack(want), spec, what="y_perm")
 
 
+def test_w4_grouped_ffn_extreme_activation_scales():
+    """The kernel stages activations as fp16 with a power-of-two scale per token (bf16 values
+    leave fp16's range).  Grouped rows scaled by 2^-50 .. 2^50, a row mixing 2^40 and 1, and a
+    zero row, against the oracle row by row through the grouped step (no router involved)."""
+    spec = moe_synth.LayerSpec("w4_scales", N=64, d=1024, d_ff=512, E=4, k=1, w4a16=True)
+    L = moe_synth.make_layer(spec, seed=31)
+    dev = to_dev(L)
+    w4 = moe.quantize_layer_w4(dev)
+    cfg = moe.cfg_from_spec(spec)
+    ws = moe.workspace(cfg)
+    counts = np.array([20, 0, 33, 11], np.int32)          # rows per expert, 64 in all
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = moe.moe_grouped_rows(cfg)
+    assert R >= 64
+    x = L["x"].float().clone()
+    exps = [-50, -24, -8, 0, 8, 24, 50]
+    for r in range(64):
+        x[r] *= 2.0 ** exps[r % len(exps)]
+    x[5] = L["x"][5].float()                               # one row spanning 2^40 within itself
+    x[5, : spec.d // 2] *= 2.0 ** 40                       # (h ~ 2^80 stays inside bf16)
+    x[6] = 0                                               # a zero row gives exactly zero
+    x_perm = torch.zeros((R, spec.d), dtype=torch.bfloat16)
+    x_perm[:64] = x.to(torch.bfloat16)
+    assert torch.equal(x_perm[:64].float(), x)             # the scaled rows are exact in bf16
+    row_w = torch.ones(R, dtype=torch.float32)
+    y = torch.full((R, spec.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_ffn_w4a16(cfg, x_perm.cuda(), torch.from_numpy(counts).cuda(),
+                              torch.from_numpy(offs).cuda(), row_w.cuda(), w4, y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_error(ws) == 0
+    q = W4Oracle(L)
+    want = []
+    for r in range(64):
+        e = int(np.searchsorted(offs, r, side="right") - 1)
+        o = oracle.moe_token_w4(x_perm[r], np.array([1.0], np.float32), np.array([1], np.int32),
+                                [q.routed(e)], [], 1)
+        want.append(oracle.bf16_bits_to_f32(o).astype(np.float64))
+    got = _gpu_out(y[:64])
+    assert np.all(np.isfinite(got))
+    compare_rows(got, np.stack(want), spec, what="scaled rows")
+    assert np.all(got[6] == 0)
+
+
 def test_w4_forward_empty_batch_and_repeatable():
     spec = SMALL[0]
     L = moe_synth.make_layer(spec, seed=1)
