@@ -16,7 +16,7 @@
 //   warp 0      TMA producer: x tile 128x64 and the hi/mid/lo rows 3 x 64x64 per k-block,
 //               4-stage ring (40 KB per stage, 128-byte swizzle);
 //   warp 1      TMEM allocation (512 columns: two 192-column slice accumulators) and the
-//               single MMA-issuing thread (tcgen05.mma M=128, N=192, K=16);
+//               MMA issue (tcgen05.mma M=128, N=192, K=16) from one elected lane;
 //   warps 2..9  two epilogue warpgroups, experts [0,32) and [32,64) of the tile.
 // Fused form (d not split, 192 < E <= 512): the ceil(E/64) CTAs of one token tile run as a
 // thread-block cluster.  Each CTA leaves its 128 x 64 logits in its shared memory (the drained ring); after a
@@ -146,17 +146,18 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == 0) {
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            int last_ph[RSTAGES];
-            for (int i = 0; i < RSTAGES; i++) last_ph[i] = -1;
-            bool ok = true;
-            for (int kb = kb0; kb < kb1; kb++) {
-                if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
-                    ok = false;
-                    break;
-                }
+        // TMA producer: the whole warp runs the loop and the waits, one elected lane issues
+        int s = 0;
+        uint32_t ph = 0;
+        int last_ph[RSTAGES];
+        for (int i = 0; i < RSTAGES; i++) last_ph[i] = -1;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; kb++) {
+            if (!waitw(&empty[s], ph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&full[s], RSTAGE);
                 const int kx = kb * RBK;
                 tma_load_2d(smem_u32(sA + s * RA_STAGE), &tmX, &full[s], kx, m0);
@@ -164,55 +165,68 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                 for (int p = 0; p < 3; p++)
                     tma_load_2d(smem_u32(sB + s * RB_STAGE + p * RB_PART), &tmW, &full[s], kx,
                                 p * E + e0);
-                last_ph[s] = (int)ph;
-                if (++s == RSTAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
-            if (!ok)
-                for (int i = 0; i < RSTAGES; i++)
-                    if (last_ph[i] >= 0)
-                        wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
+            __syncwarp();
+            last_ph[s] = (int)ph;
+            if (++s == RSTAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
+        if (!ok && lane == 0)
+            for (int i = 0; i < RSTAGES; i++)
+                if (last_ph[i] >= 0)
+                    wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(RBM, RN);
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int sl = 0; sl < nslices && ok; sl++) {
-                const int acc = sl & 1;
-                const uint32_t aph = (uint32_t)(sl >> 1) & 1u;
-                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+        // MMA issuer: the whole warp runs the loop and the waits, one elected lane issues the
+        // MMAs and commits (a loop run by a single thread spends ~100 cycles per MMA once it
+        // waits on an mbarrier between groups); the ring descriptors advance by the slot size
+        constexpr uint32_t idesc = idesc_bf16_f32(RBM, RN);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+        uint64_t ad = ad0, bd = bd0;
+        for (int sl = 0; sl < nslices && ok; sl++) {
+            const int acc = sl & 1;
+            const uint32_t aph = (uint32_t)(sl >> 1) & 1u;
+            if (!waitw(&tempty[acc], aph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+            const int kb_beg = kb0 + sl * SLICE_KB;
+            const int kb_end = min(kb1, kb_beg + SLICE_KB);
+            for (int kb = kb_beg; kb < kb_end; kb++) {
+                if (!waitw(&full[s], ph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-                const int kb_beg = kb0 + sl * SLICE_KB;
-                const int kb_end = min(kb1, kb_beg + SLICE_KB);
-                for (int kb = kb_beg; kb < kb_end; kb++) {
-                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + s * RA_STAGE);
-                    const uint32_t b0 = smem_u32(sB + s * RB_STAGE);
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < RBK / 16; kk++)
-                        umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                        umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
                                   (kb > kb_beg || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);
-                    if (++s == RSTAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    if (kb == kb_end - 1) umma_commit(&tfull[acc]);
                 }
-                if (ok) umma_commit(&tfull[acc]);
+                __syncwarp();
+                if (++s == RSTAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                    ad = ad0;
+                    bd = bd0;
+                } else {
+                    ad += (uint64_t)(RA_STAGE >> 4);
+                    bd += (uint64_t)(RB_STAGE >> 4);
+                }
             }
+        }
+        // every MMA issued by the elected lane completes before TMEM can be released
+        if (elect_one()) {
             umma_commit(drain);
             wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
         }
