@@ -20,6 +20,14 @@
 //             mask below the lane) + earlier steps.  perm[offsets[e] + r] = f,
 //             pos[f] = kept_offsets[e] + r if r < kept[e] else -1
 //   gather  : row r of x_perm = x[row_token[r]], 16-byte vector copies, warp per row.
+// When the count blocks can all be resident at once, count, scan and scatter run as one
+// cooperative kernel (perm_fused_kernel): after a grid barrier every block reads the whole
+// per-block histogram and computes its own bases and the offsets itself, so the three passes
+// cost one launch.
+#include <cooperative_groups.h>
+#include <cstdlib>
+#include <cstring>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -143,31 +151,17 @@ perm_scan_kernel(const int32_t* __restrict__ blk_hist, int blocks, int E, int64_
     }
 }
 
-__global__ void __launch_bounds__(kPermThreads)
-perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int k,
-                    int E, const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
-                    const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_off,
-                    int32_t* __restrict__ perm, int32_t* __restrict__ pos,
-                    int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
-    extern __shared__ int cnt[];   // [kWarps][E] counts, then running bases
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
-    __syncthreads();
-    int64_t f0 = 0;
-    const int spw = warp_slots(A, &f0);
-    warp_count(idx, A, E, f0, spw, cnt + warp * E, nullptr);
-    __syncthreads();
-    // per expert: exclusive scan over warps, starting at this block's base
-    for (int e = threadIdx.x; e < E; e += kPermThreads) {
-        int run = blk_base[(int64_t)blockIdx.x * E + e];
-        for (int wv = 0; wv < kWarps; wv++) {
-            int c = cnt[wv * E + e];
-            cnt[wv * E + e] = run;
-            run += c;
-        }
-    }
-    __syncthreads();
-    int* base = cnt + warp * E;
+// Scatter of this block's slots given the per-warp run bases in cnt[warp][e] and the offsets,
+// kept counts and kept offsets per expert (shared by perm_scatter_kernel and perm_fused_kernel).
+__device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ idx,
+                                              const float* __restrict__ w, int64_t A, int k, int E,
+                                              int64_t f0, int spw, int* base,
+                                              const int32_t* offsets, const int32_t* kept,
+                                              const int32_t* kept_off, int32_t* __restrict__ perm,
+                                              int32_t* __restrict__ pos,
+                                              int32_t* __restrict__ row_token,
+                                              float* __restrict__ row_weight) {
+    const int lane = threadIdx.x & 31;
     const unsigned lt = (1u << lane) - 1u;
     for (int step = 0; step < spw / 32; step++) {
         int64_t f = f0 + step * 32 + lane;
@@ -198,6 +192,121 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int k,
+                    int E, const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+                    const int32_t* __restrict__ kept, const int32_t* __restrict__ kept_off,
+                    int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+                    int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
+    extern __shared__ int cnt[];   // [kWarps][E] counts, then running bases
+    const int warp = threadIdx.x / 32;
+    for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    int64_t f0 = 0;
+    const int spw = warp_slots(A, &f0);
+    warp_count(idx, A, E, f0, spw, cnt + warp * E, nullptr);
+    __syncthreads();
+    // per expert: exclusive scan over warps, starting at this block's base
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        int run = blk_base[(int64_t)blockIdx.x * E + e];
+        for (int wv = 0; wv < kWarps; wv++) {
+            int c = cnt[wv * E + e];
+            cnt[wv * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    scatter_slots(idx, w, A, k, E, f0, spw, cnt + warp * E, offsets, kept, kept_off, perm, pos,
+                  row_token, row_weight);
+}
+
+// count -> grid barrier -> scan -> scatter in one cooperative launch (every block resident).
+// Shared memory: cnt [kWarps][E], then base, off, kept, koff [E] each.
+__global__ void __launch_bounds__(kPermThreads)
+perm_fused_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int k,
+                  int E, int64_t cap, int32_t* __restrict__ blk_hist, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ kept,
+                  int32_t* __restrict__ kept_off, int32_t* __restrict__ perm,
+                  int32_t* __restrict__ pos, int32_t* __restrict__ row_token,
+                  float* __restrict__ row_weight, int32_t* err) {
+    extern __shared__ int sm[];
+    int* cnt = sm;
+    int* s_base = cnt + kWarps * E;
+    int* s_off = s_base + E;
+    int* s_kept = s_off + E;
+    int* s_koff = s_kept + E;
+    __shared__ int tmp[33];
+    const int warp = threadIdx.x / 32;
+    for (int i = threadIdx.x; i < kWarps * E; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    int64_t f0 = 0;
+    const int spw = warp_slots(A, &f0);
+    warp_count(idx, A, E, f0, spw, cnt + warp * E, err);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        int sum = 0;
+        for (int wv = 0; wv < kWarps; wv++) sum += cnt[wv * E + e];
+        blk_hist[(int64_t)blockIdx.x * E + e] = sum;
+    }
+    cooperative_groups::this_grid().sync();
+    // this block's base per expert (blocks before it) and the totals; thread t owns the
+    // contiguous experts [t per, (t + 1) per), so the scans below run in expert order
+    const int nb = (int)gridDim.x;
+    const int per = (E + kPermThreads - 1) / kPermThreads;
+    const int e_lo = min(E, (int)threadIdx.x * per), e_hi = min(E, e_lo + per);
+    int loc_c = 0, loc_k = 0;
+    for (int e = e_lo; e < e_hi; e++) {
+        int before = 0, total = 0;
+        for (int b = 0; b < nb; b++) {
+            const int h = __ldcg(blk_hist + (int64_t)b * E + e);
+            if (b < (int)blockIdx.x) before += h;
+            total += h;
+        }
+        s_base[e] = before;
+        s_off[e] = total;
+        const int kp = (cap >= 0 && total > cap) ? (int)cap : total;
+        s_kept[e] = kp;
+        loc_c += total;
+        loc_k += kp;
+    }
+    int tot_c, tot_k;
+    const int ex_c = block_exclusive_scan(loc_c, tmp, &tot_c);
+    const int ex_k = block_exclusive_scan(loc_k, tmp, &tot_k);
+    {
+        int rc = ex_c, rk = ex_k;
+        for (int e = e_lo; e < e_hi; e++) {
+            const int c = s_off[e], kp = s_kept[e];
+            s_off[e] = rc;
+            s_koff[e] = rk;
+            if (blockIdx.x == 0) {
+                counts[e] = c;
+                offsets[e] = rc;
+                kept[e] = kp;
+                kept_off[e] = rk;
+            }
+            rc += c;
+            rk += kp;
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        offsets[E] = tot_c;
+        kept_off[E] = tot_k;
+    }
+    __syncthreads();
+    // per expert: exclusive scan over warps, starting at this block's base
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        int run = s_base[e];
+        for (int wv = 0; wv < kWarps; wv++) {
+            int c = cnt[wv * E + e];
+            cnt[wv * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    scatter_slots(idx, w, A, k, E, f0, spw, cnt + warp * E, s_off, s_kept, s_koff, perm, pos,
+                  row_token, row_weight);
 }
 
 // x_perm[r] = x[row_token[r]] for r < kept_off[E]; one warp per row, 16-byte vectors.
@@ -237,13 +346,90 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_
     }
 }
 
+// Blocks of perm_fused_kernel the GPU holds at once (per device and shared-memory size); 0 with
+// MOE_PERMUTE=unfused (read once per process), which keeps the three-launch form for comparisons.
+int fused_capacity(size_t smem) {
+    static int unfused = -1;
+    if (unfused < 0) {
+        const char* v = getenv("MOE_PERMUTE");
+        unfused = (v && strcmp(v, "unfused") == 0) ? 1 : 0;
+    }
+    if (unfused) return 0;
+    static int cached_dev[64][2] = {};            // {smem + 1, capacity}
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached_dev[dev][0] == (int)smem + 1) return cached_dev[dev][1];
+    int per_sm = 0;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(perm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, perm_fused_kernel, kPermThreads,
+                                                      smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int capn = per_sm * device_sm_count();
+    cached_dev[dev][0] = (int)smem + 1;
+    cached_dev[dev][1] = capn;
+    return capn;
+}
+
 }  // namespace
+
+cudaError_t launch_permute_unfused(const moe_cfg& c, const int32_t* idx, const float* w,
+                                   int32_t* counts, int32_t* offsets, int32_t* kept,
+                                   int32_t* kept_off, int32_t* perm, int32_t* pos,
+                                   int32_t* row_token, float* row_weight, int32_t* blk_hist,
+                                   int32_t* blk_base, int32_t* err, cudaStream_t s);
 
 cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w, const void* x,
                            int32_t* counts, int32_t* offsets, int32_t* kept, int32_t* kept_off,
                            int32_t* perm, int32_t* pos, int32_t* row_token, float* row_weight,
                            void* x_perm, int32_t* blk_hist, int32_t* blk_base, int32_t* err,
                            cudaStream_t s) {
+    const int64_t A = c.N * c.k;
+    const int E = c.E;
+    const int blocks = perm_blocks(A);
+    const size_t fused_smem = sizeof(int) * (kWarps + 4) * E;
+    if (blocks > 0 && blocks <= fused_capacity(fused_smem)) {
+        int64_t cap = capacity(c);
+        int k = c.k, e = E;
+        void* args[] = {(void*)&idx, (void*)&w, (void*)&A, (void*)&k, (void*)&e, (void*)&cap,
+                        (void*)&blk_hist, (void*)&counts, (void*)&offsets, (void*)&kept,
+                        (void*)&kept_off, (void*)&perm, (void*)&pos, (void*)&row_token,
+                        (void*)&row_weight, (void*)&err};
+        cudaError_t ef = cudaLaunchCooperativeKernel((const void*)perm_fused_kernel, dim3(blocks),
+                                                     dim3(kPermThreads), args, fused_smem, s);
+        if (ef != cudaSuccess) return ef;
+    } else {
+        cudaError_t eu = launch_permute_unfused(c, idx, w, counts, offsets, kept, kept_off, perm,
+                                                pos, row_token, row_weight, blk_hist, blk_base,
+                                                err, s);
+        if (eu != cudaSuccess) return eu;
+    }
+    if (blocks == 0 || x_perm == nullptr) return cudaSuccess;
+    {
+        const int esz = c.act_dtype == MOE_BF16 ? 2 : 4;
+        const int row_vecs = (int)((int64_t)c.d * esz / 16);
+        const int64_t rows = grouped_rows(c);
+        int64_t want = (rows + 7) / 8;     // 8 warps per block
+        int gblocks = (int)(want < 148 * 16 ? want : 148 * 16);
+        if (gblocks < 1) gblocks = 1;
+        gather_rows_kernel<<<gblocks, 256, 0, s>>>((const uint4*)x, row_token, kept_off + E, c.N,
+                                                   row_vecs, (uint4*)x_perm, err);
+    }
+    return cudaGetLastError();
+}
+
+// The three-launch form (count, one-block scan, scatter), for grids too large to be resident.
+cudaError_t launch_permute_unfused(const moe_cfg& c, const int32_t* idx, const float* w,
+                                   int32_t* counts, int32_t* offsets, int32_t* kept,
+                                   int32_t* kept_off, int32_t* perm, int32_t* pos,
+                                   int32_t* row_token, float* row_weight, int32_t* blk_hist,
+                                   int32_t* blk_base, int32_t* err, cudaStream_t s) {
     const int64_t A = c.N * c.k;
     const int E = c.E;
     const int blocks = perm_blocks(A);
@@ -260,16 +446,6 @@ cudaError_t launch_permute(const moe_cfg& c, const int32_t* idx, const float* w,
     perm_scatter_kernel<<<blocks, kPermThreads, smem, s>>>(idx, w, A, c.k, E, blk_base, offsets,
                                                            kept, kept_off, perm, pos, row_token,
                                                            row_weight);
-    cudaError_t e3 = cudaGetLastError();
-    if (e3 != cudaSuccess || x_perm == nullptr) return e3;
-    const int esz = c.act_dtype == MOE_BF16 ? 2 : 4;
-    const int row_vecs = (int)((int64_t)c.d * esz / 16);
-    const int64_t rows = grouped_rows(c);
-    int64_t want = (rows + 7) / 8;     // 8 warps per block
-    int gblocks = (int)(want < 148 * 16 ? want : 148 * 16);
-    if (gblocks < 1) gblocks = 1;
-    gather_rows_kernel<<<gblocks, 256, 0, s>>>((const uint4*)x, row_token, kept_off + E, c.N,
-                                               row_vecs, (uint4*)x_perm, err);
     return cudaGetLastError();
 }
 

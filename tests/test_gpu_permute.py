@@ -1,6 +1,12 @@
 """GPU parity of moe_permute (histogram, prefix sums, stable scatter, capacity, row gather)
 against the oracle's counting sort, through the C ABI.  All outputs are integers or copies, so
-every comparison is bit-exact.  The routing fed in is the oracle's own (or a synthetic one)."""
+every comparison is bit-exact.  The routing fed in is the oracle's own (or a synthetic one).
+The grouping runs as one cooperative kernel when its blocks fit on the GPU at once (every case
+here); the three-launch form is run on the same cases in a child process (MOE_PERMUTE=unfused)."""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -59,6 +65,8 @@ def _permute(N, k, E, idx, cf=0.0, d=64, dtype=moe.MOE_BF16, seed=0):
     (5, 3, 3, 0.0, 0.0),               # k = E
     (1025, 2, 16, 0.0, 0.0),           # last block of 2 slots: most of its warps get none
     (4101, 2, 64, 1.0, 1.0),           # 4 full blocks and a 10-slot one, with capacity
+    (16384, 8, 128, 1.25, 1.2),        # the Qwen-shaped layer's grouping: 64 blocks
+    (65536, 8, 256, 0.0, 0.0),         # 256 blocks in one cooperative grid
 ])
 def test_permute_matches_oracle(N, k, E, cf, skew):
     idx = _random_idx(N * 7 + E, N, k, E, skew)
@@ -114,3 +122,13 @@ def test_permute_is_deterministic():
     b = _permute(4096, 8, 256, idx)[0]
     for key in a:
         assert torch.equal(a[key], b[key]), key
+
+
+def test_three_launch_form_matches_oracle():
+    """The count / scan / scatter kernels the cooperative kernel replaces, on the same cases."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, MOE_PERMUTE="unfused")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_permute.py"),
+                        "-q", "-x", "-m", "gpu", "-k", "not three_launch"],
+                       env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
