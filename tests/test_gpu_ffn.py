@@ -16,7 +16,7 @@ from gpu_util import ExpertCache, compare_rows, dtype_code, out_f64
 pytestmark = pytest.mark.gpu
 
 
-def _grouped(spec, rows_per_expert, seed=0):
+def _grouped(spec, rows_per_expert, seed=0, check_rows=None):
     E = spec.E
     L = moe_synth.make_layer(spec.with_(N=1), seed=seed)
     R = int(sum(rows_per_expert))
@@ -39,13 +39,14 @@ def _grouped(spec, rows_per_expert, seed=0):
     # oracle: one expert, one token, weight row_w[r]
     cache = ExpertCache(dev)
     code = dtype_code(spec)
-    ref = np.zeros((R, spec.d))
-    for e in range(E):
-        for r in range(int(kept_off[e]), int(kept_off[e + 1])):
-            o = oracle.moe_token(x_perm[r], np.array([row_w[r]], np.float32), np.array([1]),
-                                 [cache.routed(e)], [], code, 1 if code == oracle.BF16 else 0)
-            ref[r] = out_f64(o, spec)
-    return out_f64(y[:R], spec), ref
+    rows = range(R) if check_rows is None else check_rows
+    ref = np.zeros((len(rows), spec.d))
+    for i, r in enumerate(rows):
+        e = int(np.searchsorted(kept_off.numpy(), r, side="right") - 1)
+        o = oracle.moe_token(x_perm[r], np.array([row_w[r]], np.float32), np.array([1]),
+                             [cache.routed(e)], [], code, 1 if code == oracle.BF16 else 0)
+        ref[i] = out_f64(o, spec)
+    return out_f64(y[torch.as_tensor(list(rows), dtype=torch.long)], spec), ref
 
 
 @pytest.mark.parametrize("d,F,rows", [
@@ -55,6 +56,37 @@ def _grouped(spec, rows_per_expert, seed=0):
     (1024, 1024, [256, 257, 3]),
 ])
 def test_grouped_ffn_bf16(d, F, rows):
+    _check_grouped_ffn_bf16(d, F, rows)
+
+
+def test_grouped_ffn_more_tiles_than_pairs():
+    """More tiles than CTA pairs in both GEMMs (120 gate/up and 160 down tiles of 130-row chunks
+    over 74 pairs), so every pair runs several tiles: both TMEM accumulators, their full/empty
+    phases and the rings' phases across tiles.  Checked rows: each chunk's first and last row
+    and a seeded sample."""
+    spec = moe_synth.LayerSpec("g", N=1, d=2048, d_ff=768, E=10, k=1)
+    rows = [260] * 10                       # two chunks of 130 rows (MMA N = 144) per expert
+    rng = np.random.default_rng(7)
+    check = set()
+    for e in range(10):
+        base = 260 * e
+        check.update((base, base + 129, base + 130, base + 259))
+    check.update(rng.choice(2600, 24, replace=False).tolist())
+    check = sorted(check)
+    got, ref = _grouped(spec, rows, seed=3, check_rows=check)
+    compare_rows(got, ref, spec, what="grouped ffn, several tiles per pair")
+
+
+def test_grouped_ffn_decode_variant_many_tiles():
+    """The decode-sized variant (at most 64 rows in all, 32-row token slots) with 1024 tiles per
+    GEMM: 64 one-row experts, d = 4096, d_ff = 2048 (16 weight tiles per chunk in both GEMMs),
+    every row checked."""
+    spec = moe_synth.LayerSpec("g", N=1, d=4096, d_ff=2048, E=64, k=1)
+    got, ref = _grouped(spec, [1] * 64, seed=5)
+    compare_rows(got, ref, spec, what="grouped ffn, decode variant")
+
+
+def _check_grouped_ffn_bf16(d, F, rows):
     spec = moe_synth.LayerSpec("g", N=1, d=d, d_ff=F, E=len(rows), k=1)
     got, ref = _grouped(spec, rows, seed=d + F)
     compare_rows(got, ref, spec, what="grouped ffn")
