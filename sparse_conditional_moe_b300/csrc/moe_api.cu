@@ -1,5 +1,6 @@
 // moe_api.cu -- the C ABI of libmoe.so: argument validation, workspace layout and the order of
 // launches for each entry point declared in include/moe.h.
+#include <atomic>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -23,16 +24,16 @@ struct NvtxRange {
 };
 
 int device_sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];       // per device; 0 until first asked
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 // The bf16 forward's grouped GEMMs run on the CTA-pair kernels of grouped_gemm_pair.cu;

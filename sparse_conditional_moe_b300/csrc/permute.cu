@@ -25,6 +25,8 @@
 // per-block histogram and computes its own bases and the offsets itself, so the three passes
 // cost one launch.
 #include <cooperative_groups.h>
+
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -348,17 +350,20 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_
 
 // Blocks of perm_fused_kernel the GPU holds at once (per device and shared-memory size); 0 with
 // MOE_PERMUTE=unfused (read once per process), which keeps the three-launch form for comparisons.
+// The cache holds (shared-memory bytes, capacity) in one atomic word per device, so threads
+// forwarding at once never see one call's size with another's capacity.
 int fused_capacity(size_t smem) {
-    static int unfused = -1;
-    if (unfused < 0) {
+    static std::atomic<int> unfused{-1};
+    if (unfused.load(std::memory_order_relaxed) < 0) {
         const char* v = getenv("MOE_PERMUTE");
-        unfused = (v && strcmp(v, "unfused") == 0) ? 1 : 0;
+        unfused.store((v && strcmp(v, "unfused") == 0) ? 1 : 0, std::memory_order_relaxed);
     }
-    if (unfused) return 0;
-    static int cached_dev[64][2] = {};            // {smem + 1, capacity}
+    if (unfused.load(std::memory_order_relaxed)) return 0;
+    static std::atomic<uint64_t> cached[64];                // (smem << 32) | capacity, 0 = none
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached_dev[dev][0] == (int)smem + 1) return cached_dev[dev][1];
+    const uint64_t hit = cached[dev].load(std::memory_order_acquire);
+    if (hit != 0 && (hit >> 32) == (uint64_t)smem) return (int)(hit & 0xffffffffu);
     int per_sm = 0;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(perm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -372,8 +377,7 @@ int fused_capacity(size_t smem) {
         return 0;
     }
     const int capn = per_sm * device_sm_count();
-    cached_dev[dev][0] = (int)smem + 1;
-    cached_dev[dev][1] = capn;
+    cached[dev].store(((uint64_t)smem << 32) | (uint32_t)capn, std::memory_order_release);
     return capn;
 }
 

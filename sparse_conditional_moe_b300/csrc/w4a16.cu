@@ -17,6 +17,7 @@
 // Every code byte of a touched expert is read once per pass of 8 token rows, so for decode (a
 // few rows per expert) the expert weights cost a quarter of their bf16 bytes plus 1/32 for
 // scales.
+#include <atomic>
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -455,12 +456,15 @@ cudaError_t launch_w4mma(const W4Group& g, const __nv_bfloat16* A, int K, const 
     if (!make_code_map(&m0, M0.q, wrows, K) || !make_code_map(&m1, NM == 2 ? M1.q : M0.q, wrows, K) ||
         !make_scale_map(&s0, M0.s, wrows, K) || !make_scale_map(&s1, NM == 2 ? M1.s : M0.s, wrows, K))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
+    // the shared-memory opt-in is per device: remember it per device
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(w4_mma_kernel<NM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
     }
     W4MmaArgs a{g.G, g.rows, g.row_off, g.uniform_rows, g.a_stride, g.c_stride, A, K,
                 J, row_scale, C, err};
