@@ -39,6 +39,8 @@ from sparse_conditional_moe_b300 import accounting  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 HEADLINE = moe_synth.DSV3_PREFILL
+# the layer whose backward is timed in a full run (its backward is checked at full size)
+BACKWARD_WORKLOAD = moe_synth.MIXTRAL
 SIDE_WORKLOADS = (moe_synth.MIXTRAL, moe_synth.DSV3_DECODE, moe_synth.DSV3_DECODE_W4,
                   moe_synth.QWEN3_SKEWED)
 # the library forks the shared experts of bf16 batches of at most this many tokens onto its
@@ -357,10 +359,49 @@ def count_kernel_launches(torch, lay, x) -> int:
 
 # ------------------------------------------------------------------ one workload
 
-def measure(spec, args, peaks, torch, dist, world, rank, local, headline: bool):
+def backward_eligible(spec) -> bool:
+    """moe_backward covers bf16 layers with d a multiple of 64 and d_ff, d_ff_shared multiples of
+    128 (not W4A16 weights)."""
+    return (spec.dtype == "bf16" and not spec.w4a16 and spec.d % 64 == 0 and spec.d_ff % 128 == 0
+            and (spec.n_shared == 0 or spec.d_ff_shared % 128 == 0))
+
+
+def measure_backward(spec, lay, x, kept_rows, iters, peaks, torch, world):
+    """moe_backward after one forward: 2 warm-up passes, then `iters` passes between CUDA events
+    on the launching stream.  Algorithmic expert work of a backward pass: the data and weight
+    gradients of the three expert matrices, 12 d d_ff per kept row (twice the forward's 6; the
+    pass also recomputes gate/up, 4 d d_ff per row, not counted), and the same for the shared
+    experts over every token."""
+    dout = torch.randn(lay.out.shape, device="cuda").to(torch.bfloat16)
+    lay.forward(x)
+    for _ in range(2):
+        lay.backward(dout)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(iters):
+        lay.backward(dout)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    if lay.device_error() != 0:
+        raise RuntimeError(f"device error in the backward pass ({spec.name})")
+    ms = b0.elapsed_time(b1) / iters
+    flops = 12.0 * spec.d * spec.d_ff * kept_rows + 12.0 * spec.d * spec.d_ff_shared * spec.N * spec.n_shared
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"ms": ms, "tokens_per_s": spec.N * world / (ms / 1e3), "iterations": iters,
+            "expert_tflops": tflops, "tensor_frac": tflops / peaks["bf16_tflops"],
+            "work": f"12*d*d_ff*kept_rows (+ shared) = {flops:.4g} flop",
+            "note": "moe_backward after one forward: dx, dW_r, db and the expert weight gradients, "
+                    "all fp32; gate/up recomputed (not counted)"}
+
+
+def measure(spec, args, peaks, torch, dist, world, rank, local, headline: bool,
+            backward: bool = False):
     """Device-timed forward of one workload: K steps after W warm-up steps, events around the
     routed gate/up and down GEMMs of every timed step, clocks sampled during the region.
-    The headline workload also gets the end-to-end measurement and the CPU oracle leg."""
+    The headline workload also gets the end-to-end measurement and the CPU oracle leg;
+    `backward` adds a timed moe_backward (measure_backward)."""
     from sparse_conditional_moe_b300 import moe
     dev = moe_synth.make_layer(spec, seed=0, device="cuda")
     cfg = moe.cfg_from_spec(spec)
@@ -452,6 +493,9 @@ def measure(spec, args, peaks, torch, dist, world, rank, local, headline: bool):
                          "not bracketed by the caller-stream events)") if forked else None,
         "clocks": clk,
     }
+    if backward and args.backward > 0 and backward_eligible(spec):
+        out["backward"] = measure_backward(spec, lay, xs[0], kept_rows, args.backward, peaks,
+                                           torch, world)
     if not headline:
         del lay, dev, xs, w4
         torch.cuda.empty_cache()
@@ -630,6 +674,10 @@ def main():
                     help="override the batch size N (smaller cases for profiling; not a bench line)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count E (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--backward", type=int, default=5,
+                    help="timed moe_backward passes after the forward measurement of the "
+                         "Mixtral-shaped layer (also when it is run alone, at any --tokens / "
+                         "--experts); 0: none")
     ap.add_argument("--no-workloads", action="store_true",
                     help="measure the named workload only (no `workloads` object)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -658,13 +706,16 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res = measure(spec, args, peaks, torch, dist, world, rank, local, headline=True)
+    single = args.no_workloads or args.tokens > 0 or args.experts > 0
+    res = measure(spec, args, peaks, torch, dist, world, rank, local, headline=True,
+                  backward=spec.name.startswith(BACKWARD_WORKLOAD.name))
     side = {}
-    if not args.no_workloads and args.tokens == 0 and args.experts == 0:
+    if not single:
         for s in SIDE_WORKLOADS:
             if s.name == spec.name:
                 continue
-            r = measure(s, args, peaks, torch, dist, world, rank, local, headline=False)
+            r = measure(s, args, peaks, torch, dist, world, rank, local, headline=False,
+                        backward=s.name == BACKWARD_WORKLOAD.name)
             side[s.name] = {"ms_per_step": r["ms_per_step"], "value": r["value"],
                             "unit": "tokens/s", "gateup": r["gateup"], "down": r["down"],
                             "layer_roofline_frac": r["layer"]["roofline_frac"],
@@ -675,6 +726,8 @@ def main():
                             "clocks": {k: r["clocks"].get(k) for k in
                                        ("sm_mhz", "sm_min_mhz", "samples", "reasons")},
                             "config": config_of(s, world)}
+            if r.get("backward"):
+                side[s.name]["backward"] = r["backward"]
 
     if rank == 0:
         per_step = res.get("gpu_launches_per_step", -1)
@@ -698,6 +751,8 @@ def main():
             "cpu_baseline_one_core": res.get("cpu_baseline_one_core"),
             "workloads": side or None,
         }
+        if res.get("backward"):
+            line["backward"] = res["backward"]
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
