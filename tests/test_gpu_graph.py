@@ -1,7 +1,8 @@
 """The forward pass under CUDA-graph capture: a captured moe_forward replays to the same bytes
 as the eager call.  This covers the decode path that forks the shared experts onto the
-library's own stream (the fork and join become graph edges), the W4A16 forward and a layer with
-capacity dropping.  No launch inside the forward allocates, synchronises or reads back, which is
+library's own stream (the fork and join become graph edges), the W4A16 forward, layers with
+capacity dropping, the tensor-core router's cluster launch and the permutation's cooperative
+launch.  No launch inside the forward allocates, synchronises or reads back, which is
 what capture requires."""
 import pytest
 import torch
@@ -20,6 +21,13 @@ CASES = [
                         d_ff_shared=128, capacity_factor=1.0),
     moe_synth.LayerSpec("decode_w4", N=32, d=512, d_ff=256, E=16, k=4, n_shared=1,
                         d_ff_shared=256, w4a16=True),
+    # the tensor-core router in its fused cluster form (E = 256, batch over 1024 tokens) and in
+    # its unfused form with the top-k kernel (E = 128); every case groups its assignments with
+    # the cooperative permutation kernel
+    moe_synth.LayerSpec("fused_router", N=1100, d=512, d_ff=256, E=256, k=8, n_shared=1,
+                        d_ff_shared=256),
+    moe_synth.LayerSpec("tc_router_capacity", N=2048, d=512, d_ff=256, E=128, k=4,
+                        capacity_factor=1.25, zipf_bias=1.2),
 ]
 
 
