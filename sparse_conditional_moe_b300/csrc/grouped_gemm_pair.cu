@@ -19,7 +19,7 @@
 // multiply-adds (a single-CTA 128 x 256 tile needs 48 KB for the same work), and 192 KB of
 // shared memory hold 7 weight and 5 token k-blocks.
 //
-// Roles (352 threads per CTA, one CTA per SM, persistent over the pair's tiles):
+// Roles (384 threads per CTA, one CTA per SM, persistent over the pair's tiles):
 //   warp 0      weight producer in each CTA: its weight rows into the weight ring (TMA); both
 //               CTAs' copies complete on the leader CTA's barrier;
 //   warp 10     token producer in each CTA: its half of the chunk's token rows into the token
@@ -31,7 +31,10 @@
 //   warps 2..9  epilogue in each CTA, two warps per TMEM lane quarter taking alternate 32-token
 //               chunks (short tiles are otherwise bound by the epilogue): tcgen05.ld of its 128
 //               weight rows, silu*mul or scale in fp32, one rounding to bf16, stores through
-//               shared memory and TMA.
+//               shared memory and TMA;
+//   warp 11     tile scheduler in each CTA: decodes the pair's tiles (group, chunk, weight
+//               tile, token rows) into a 4-entry queue in shared memory that the producers, the
+//               MMA warp and the down GEMM's epilogue read.
 // Gate/up: each CTA's 128 weight rows are 64 gate rows followed by the matching 64 up rows (two
 // TMA boxes per k-block: every copy instruction has a fixed cost in the copy engine, so boxes stay
 // large), so TMEM lanes 0-63 hold gate and lanes 64-127 up projections of the same 64 hidden
@@ -63,7 +66,10 @@ constexpr int A_STAGE = WROWS * BK * 2;    // 16 KB
 constexpr uint32_t TMEM_COLS = 2 * TOK_MAX;
 constexpr int EPI_WARPS = 8;
 constexpr int TOK_WARP = 2 + EPI_WARPS;    // the token producer, after the epilogue warps
-constexpr int NUM_THREADS = 32 * (TOK_WARP + 1);
+constexpr int SCHED_WARP = TOK_WARP + 1;   // the tile scheduler
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
+constexpr int QDEPTH = 4;                  // decoded tiles the scheduler may run ahead
+constexpr int TQ_BYTES = 256;              // the decoded-tile queue (QDEPTH PTile entries)
 // Epilogue shared memory: down = 8 warps x 2 staging buffers x 2 KB; gate/up = 4 exchange buffers
 // (32 lanes x 32 floats, one per warp pair) + 4 gate warps x 2 staging buffers x 2 KB; + flags.
 constexpr int EPI_BYTES = 32768 + 256;
@@ -85,10 +91,10 @@ struct PairCfg {
     static constexpr int A_STAGES = TOK_SLOT >= 128 ? 7 : 10;
     static constexpr int B_STAGES = TOK_SLOT >= 128 ? 5 : 8;
     static constexpr int RING_BYTES = A_STAGES * A_STAGE + B_STAGES * B_STAGE;
-    static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + 1024 + 512;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + 1024 + 512 + TQ_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
     static_assert(B_STAGE % 1024 == 0, "stages stay 1 KB aligned for the 128-byte swizzle");
-    static_assert((2 * A_STAGES + 2 * B_STAGES + 5) * 8 + 8 <= 512, "barriers fit their area");
+    static_assert((2 * A_STAGES + 2 * B_STAGES + 5 + 2 * QDEPTH) * 8 + 8 <= 512, "barriers fit their area");
 };
 
 struct TokMaps {
@@ -123,12 +129,19 @@ struct PTile {
     int64_t c_row0;    // output row of the chunk's first row
 };
 
+static_assert(QDEPTH * sizeof(PTile) <= TQ_BYTES, "the tile queue fits its area");
+
 __device__ __forceinline__ int total_tiles(const PairParams& p) {
     if (p.rows == nullptr) return p.G * ((p.uniform_rows + TOK_MAX - 1) / TOK_MAX) * p.n_wt;
     return p.chunk_off[p.G] * p.n_wt;
 }
 
-__device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile) {
+// Called by all 32 lanes of a warp with the same tile.  The group is found by a 32-way search
+// over chunk_off: each level is one coalesced load per lane and a ballot (two levels cover 1024
+// groups), and the last level also loads every candidate's row count and row offset, so a tile
+// costs two rounds of loads instead of the ten dependent ones of a binary search (measured at
+// 1.4-1.8k cycles per tile in every role, a sixth of a short tile's time).
+__device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile, int lane) {
     PTile t;
     int nch, n, local;
     int64_t a0, c0;
@@ -141,18 +154,35 @@ __device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile) {
         a0 = (int64_t)t.g * p.a_stride;
         c0 = (int64_t)t.g * p.c_stride;
     } else {
-        // largest g with chunk_off[g] * n_wt <= tile (that group is non-empty)
+        // the largest g with chunk_off[g] * n_wt <= tile (that group is non-empty); it lies in
+        // [lo, hi), and chunk_off[lo] * n_wt <= tile holds throughout (chunk_off[0] = 0)
         int lo = 0, hi = p.G;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.chunk_off[mid] * p.n_wt <= tile) lo = mid;
-            else hi = mid;
+        while (hi - lo > 32) {
+            const int step = (hi - lo + 31) >> 5;
+            const int i = lo + lane * step;
+            const bool le = i < hi && p.chunk_off[i] * p.n_wt <= tile;
+            const int L = 31 - __clz(__ballot_sync(0xffffffffu, le));   // lane 0 always holds
+            lo += L * step;
+            hi = min(hi, lo + step);
         }
+        const int i = lo + lane;
+        int off0 = 0, off1 = 0, rows = 0, roff = 0;
+        if (i < hi) {
+            const int g = p.zigzag ? zigzag_group(i, p.G) : i;
+            off0 = p.chunk_off[i];
+            off1 = p.chunk_off[i + 1];
+            rows = p.rows[g];
+            roff = p.row_off[g];
+        }
+        const int L = 31 - __clz(__ballot_sync(0xffffffffu, i < hi && off0 * p.n_wt <= tile));
+        lo += L;
+        off0 = __shfl_sync(0xffffffffu, off0, L);
+        off1 = __shfl_sync(0xffffffffu, off1, L);
+        n = __shfl_sync(0xffffffffu, rows, L);
+        a0 = c0 = __shfl_sync(0xffffffffu, roff, L);
         t.g = p.zigzag ? zigzag_group(lo, p.G) : lo;
-        nch = p.chunk_off[lo + 1] - p.chunk_off[lo];
-        local = tile - p.chunk_off[lo] * p.n_wt;
-        n = p.rows[t.g];
-        a0 = c0 = p.row_off[t.g];
+        nch = off1 - off0;
+        local = tile - off0 * p.n_wt;
     }
     raster_tile(local, nch, p.n_wt, t.c, t.w);
     // the group's rows split evenly over its chunks: the first n % nch chunks get one more
@@ -165,6 +195,23 @@ __device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile) {
     t.a_row0 = a0 + start;
     t.c_row0 = c0 + start;
     return t;
+}
+
+// The decoded-tile queue.  The scheduler warp pushes each of the pair's tiles (in the order every
+// role walks them) and then an end marker (g < 0); a reader warp takes the next entry and frees
+// the slot.  Returns 1 for a tile, 0 at the end, -1 when a wait gave up (abort).
+__device__ __forceinline__ int pop_tile(const PTile* tq, uint64_t* q_full, uint64_t* q_empty, int& s,
+                                        uint32_t& ph, PTile& t, volatile int* abort_flag) {
+    if (!waitw(&q_full[s], ph, abort_flag)) return -1;
+    t = tq[s];
+    __syncwarp();
+    if (elect_one()) mbar_arrive(&q_empty[s]);
+    __syncwarp();
+    if (++s == QDEPTH) {
+        s = 0;
+        ph ^= 1u;
+    }
+    return t.g >= 0 ? 1 : 0;
 }
 
 // silu(z) = z / (1 + e^-z) with the hardware exponential and division: their relative error
@@ -210,8 +257,11 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
     uint64_t* tfull = empty_b + SB;        // [2] both: accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] leader: both CTAs' epilogues drained it
     uint64_t* drain = tempty + 2;          // [1] leader: MMA drain on exit
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* q_full = drain + 1;          // [QDEPTH] a decoded tile is in the queue slot
+    uint64_t* q_empty = q_full + QDEPTH;   // [QDEPTH] every consumer has read the slot
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + QDEPTH);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    PTile* tq = reinterpret_cast<PTile*>(reinterpret_cast<uint8_t*>(bars) + 512);   // [QDEPTH]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -232,6 +282,13 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
             mbar_init(&tempty[a], 2 * EPI_WARPS);   // every epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
+        // the queue's readers: both producers, the MMA warp (leader CTA) and, in the down GEMM,
+        // the epilogue warps (the gate/up epilogue paces its warp pairs itself, see below)
+        const int readers = 2 + (leader ? 1 : 0) + (EPI == EPI_SCALE ? EPI_WARPS : 0);
+        for (int i = 0; i < QDEPTH; i++) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], readers);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmW0);
@@ -262,12 +319,16 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
         const int nst = wts ? SA : SB;
         uint64_t* fullr = wts ? full_a : full_b;
         uint64_t* emptyr = wts ? empty_a : empty_b;
-        int s = 0;
-        uint32_t ph = 0;
+        int s = 0, qs = 0;
+        uint32_t ph = 0, qph = 0;
         bool ok = true;
-        for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
-            const PTile t = decode_tile(p, tile);
-            if (t.box > kMaxBox) continue;
+        while (ok) {
+            PTile t;
+            const int got = pop_tile(tq, q_full, q_empty, qs, qph, t, abort_flag);
+            if (got <= 0) {
+                ok = got == 0;
+                break;
+            }
             const int half = t.n_mma >> 1;
             const int tok_y = (int)(t.a_row0 + (int64_t)rank * half);
             const uint32_t tx = wts ? 2u * (uint32_t)A_STAGE : 2u * (uint32_t)(tok_box_rows(t.box) * BK * 2);
@@ -311,15 +372,15 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
             // The whole warp runs the loop and the waits; one elected lane issues the MMAs and
             // the commits (see elect_one).  The ring descriptors advance by adding the slot size
             // to their address field.
-            int sa = 0, sb = 0;
-            uint32_t pha = 0, phb = 0;
+            int sa = 0, sb = 0, qs = 0;
+            uint32_t pha = 0, phb = 0, qph = 0;
             bool ok = true;
             int it = 0;
             const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
             uint64_t ad = ad0, bd = bd0;
-            for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
-                const PTile t = decode_tile(p, tile);
-                if (t.box > kMaxBox) continue;
+            while (ok) {
+                PTile t;
+                if (pop_tile(tq, q_full, q_empty, qs, qph, t, abort_flag) <= 0) break;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -369,6 +430,41 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
             }
         }
         __syncwarp();
+    } else if (warp == SCHED_WARP) {
+        // ---------------------------------- tile scheduler (both CTAs): decodes each tile once,
+        // up to QDEPTH ahead of its readers (a decode is a few rounds of dependent loads and
+        // integer divisions, about a thousand cycles that the producers and the MMA warp would
+        // otherwise spend between tiles)
+        int qs = 0;
+        uint32_t qph = 0;
+        bool ok = true;
+        for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
+            const PTile t = decode_tile(p, tile, lane);
+            if (t.box > kMaxBox) {
+                if (leader && lane == 0 && p.err) atomicOr(p.err, MOE_DEVERR_BOUNDS);
+                continue;
+            }
+            if (!waitw(&q_empty[qs], qph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                tq[qs] = t;
+                mbar_arrive(&q_full[qs]);
+            }
+            __syncwarp();
+            if (++qs == QDEPTH) {
+                qs = 0;
+                qph ^= 1u;
+            }
+        }
+        if (ok && waitw(&q_empty[qs], qph ^ 1u, abort_flag)) {   // the end marker
+            if (lane == 0) {
+                tq[qs].g = -1;
+                mbar_arrive(&q_full[qs]);
+            }
+        }
+        __syncwarp();
     } else {
         // -------------------------------------------------- epilogue (warps 2..9, both CTAs)
         static_assert(TOK_WARP == 2 + EPI_WARPS, "warps 2 .. 1 + EPI_WARPS are the epilogue");
@@ -390,11 +486,8 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
             int nchunk = 0, it = 0, sent = 0;
             bool stop = false;
             for (int tile = cluster; tile < ntiles && !stop; tile += nclusters) {
-                const PTile t = decode_tile(p, tile);
-                if (t.box > kMaxBox) {
-                    if (leader && warp == 2 && lane == 0 && p.err) atomicOr(p.err, MOE_DEVERR_BOUNDS);
-                    continue;
-                }
+                const PTile t = decode_tile(p, tile, lane);
+                if (t.box > kMaxBox) continue;
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -455,8 +548,8 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_cluster(acc ? te1 : te0);
-                    if (up_warp && nch <= sub) mbar_arrive_cluster(acc ? te1 : te0);
+                    mbar_arrive_cluster_relaxed(acc ? te1 : te0);
+                    if (up_warp && nch <= sub) mbar_arrive_cluster_relaxed(acc ? te1 : te0);
                 }
             }
             if (up_warp) {   // the stop message: the gate warp leaves its loop on it
@@ -470,13 +563,28 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
             __syncwarp();
         } else {
             const uint32_t stage0 = smem_u32(sEpi) + (uint32_t)(warp - 2) * 4096u;
-            int nchunk = 0, it = 0;
-            for (int tile = cluster; tile < ntiles; tile += nclusters) {
-                const PTile t = decode_tile(p, tile);
-                if (t.box > kMaxBox) {
-                    if (leader && warp == 2 && lane == 0 && p.err) atomicOr(p.err, MOE_DEVERR_BOUNDS);
-                    continue;
+            int nchunk = 0, it = 0, qs = 0;
+            uint32_t qph = 0;
+            static_assert(TOK_MAX <= 2 * 4 * 32, "a warp takes at most 4 chunks of a tile");
+            // One tile of lookahead: the next tile is taken from the queue, and the row scales of
+            // this warp's (at most 4) chunks of it loaded, before the current tile's chunks are
+            // written, so that the loads' latency (high while the rings stream) stays hidden.
+            auto load_scales = [&](const PTile& u, float (&sc)[4]) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int r = (sub + 2 * i) * 32 + lane;
+                    sc[i] = (p.row_scale && r < u.rows) ? p.row_scale[u.c_row0 + r] : 1.f;
                 }
+            };
+            PTile t;
+            float sc[4];
+            int got = pop_tile(tq, q_full, q_empty, qs, qph, t, abort_flag);
+            if (got > 0) load_scales(t, sc);
+            while (got > 0) {
+                PTile tn;
+                float scn[4];
+                const int gotn = pop_tile(tq, q_full, q_empty, qs, qph, tn, abort_flag);
+                if (gotn > 0) load_scales(tn, scn);
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
                 ++it;
@@ -487,14 +595,9 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                 const int nch = (t.rows + 31) >> 5;
                 const int col = t.w * 256 + (int)rank * 128 + q * 32;
                 const bool warp_ok = col < p.n_out;
-#pragma unroll 1
-                for (int ch = sub; ch < nch; ch += 2, nchunk++) {
-                    uint32_t a[32];
-                    tmem_ld32(taddr + ch * 32, a);
-                    tmem_ld_wait();
+                auto emit = [&](const uint32_t (&a)[32], int ch, float s_lane) {
                     const int left = t.rows - ch * 32;
                     const int64_t gr = t.c_row0 + ch * 32;
-                    const float s_lane = (p.row_scale && lane < left) ? p.row_scale[gr + lane] : 1.f;
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; j++)
@@ -503,10 +606,29 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                         store_chunk32_t(&tmC, stage0 + (uint32_t)(nchunk & 1) * 2048u, v, left,
                                         p.C + gr * p.ldc + col + lane, p.ldc, col + lane < p.n_out,
                                         col, (int32_t)gr);
+                    ++nchunk;
+                };
+                // chunks sub, sub + 2, ...: the next chunk's TMEM load is in flight while the
+                // current one is scaled and stored (two register sets, used in turn)
+                uint32_t a0[32], a1[32];
+                if (sub < nch) tmem_ld32(taddr + sub * 32, a0);
+#pragma unroll 1
+                for (int ch = sub, i = 0; ch < nch; ch += 4, i += 2) {
+                    tmem_ld_wait();
+                    if (ch + 2 < nch) tmem_ld32(taddr + (ch + 2) * 32, a1);
+                    emit(a0, ch, i == 0 ? sc[0] : sc[2]);
+                    if (ch + 2 >= nch) break;
+                    tmem_ld_wait();
+                    if (ch + 4 < nch) tmem_ld32(taddr + (ch + 4) * 32, a0);
+                    emit(a1, ch + 2, i == 0 ? sc[1] : sc[3]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
+                if (lane == 0) mbar_arrive_cluster_relaxed(acc ? te1 : te0);
+                t = tn;
+#pragma unroll
+                for (int i = 0; i < 4; i++) sc[i] = scn[i];
+                got = gotn;
             }
             if (lane == 0) bulk_wait_all();   // staged stores done before the CTA can exit
             __syncwarp();

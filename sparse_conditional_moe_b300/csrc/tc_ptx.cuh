@@ -281,8 +281,15 @@ static __device__ __forceinline__ void cluster_sync_all() {
                      : "memory");
 }
 // Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
-static __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address) with no memory
+// ordering, for a signal that orders nothing but tcgen05 work the caller has already waited for.
+// The accumulator hand-back is one: the epilogue's tcgen05.ld have completed (tcgen05.wait::ld)
+// and been fenced (tcgen05.fence::before_thread_sync), so the MMAs that follow the wait cannot
+// touch data still being read.  A release at cluster scope would in addition wait until the
+// warp's earlier output stores are visible cluster-wide, which was measured at 2-3 thousand
+// cycles per tile while the rings stream, half the epilogue's time on short tiles.
+static __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 // TMA load into this CTA's shared memory whose completion is counted on an mbarrier that may
