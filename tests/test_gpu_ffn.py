@@ -86,6 +86,37 @@ def test_grouped_ffn_decode_variant_many_tiles():
     compare_rows(got, ref, spec, what="grouped ffn, decode variant")
 
 
+def _chunk_bounds(n, chunk_rows=256):
+    """First and last row (within the group) of every chunk of a group of n rows: the group splits
+    evenly into ceil(n / chunk_rows) chunks, the first n % chunks one row longer."""
+    if n == 0:
+        return []
+    c = -(-n // chunk_rows)
+    base, rem = divmod(n, c)
+    out, start = [], 0
+    for i in range(c):
+        r = base + (1 if i < rem else 0)
+        out += [start, start + r - 1]
+        start += r
+    return out
+
+
+def test_grouped_ffn_chunk_boundaries():
+    """Groups on both sides of the CTA-pair GEMMs' chunk boundaries (256, 512, 768 rows; chunks
+    split evenly and rounded up to 16 for the MMA's N), an empty and a one-row group.  Checked
+    rows: every chunk's first and last row and a seeded sample."""
+    rows = [255, 256, 257, 300, 0, 511, 512, 513, 777, 1, 1100, 258]
+    spec = moe_synth.LayerSpec("g", N=1, d=512, d_ff=384, E=len(rows), k=1)
+    off = np.concatenate([[0], np.cumsum(rows)])
+    check = set()
+    for e, n in enumerate(rows):
+        check.update(int(off[e] + r) for r in _chunk_bounds(n))
+    rng = np.random.default_rng(17)
+    check.update(rng.choice(int(off[-1]), 40, replace=False).tolist())
+    got, ref = _grouped(spec, rows, seed=19, check_rows=sorted(check))
+    compare_rows(got, ref, spec, what="grouped ffn, chunk boundaries")
+
+
 def _check_grouped_ffn_bf16(d, F, rows):
     spec = moe_synth.LayerSpec("g", N=1, d=d, d_ff=F, E=len(rows), k=1)
     got, ref = _grouped(spec, rows, seed=d + F)
