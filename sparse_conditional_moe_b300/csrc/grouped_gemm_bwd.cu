@@ -13,12 +13,13 @@
 // The same kernels serve the shared experts (one group of N rows each, weight 1).
 //
 // Design (one CTA per SM, persistent, warp-specialised, 192 threads), as the forward kernel:
-//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128-byte swizzle) per
-//               k-block into a 4-stage ring (48 KB per stage).  A K-major operand is one box
-//               of its rows x 64; an MN-major operand is boxes of 64 k-rows x 64 elements,
-//               8 KB apart (two for A, four for B);
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
-//               K=16) with the operands' majorness in the instruction descriptor;
+//   warp 0      TMA producer (the warp runs the loop, an elected lane issues): A tile 128x64
+//               and B tile 256x64 (bf16, 128-byte swizzle) per k-block into a 4-stage ring
+//               (48 KB per stage).  A K-major operand is one box of its rows x 64; an MN-major
+//               operand is boxes of 64 k-rows x 64 elements, 8 KB apart (two for A, four for B);
+//   warp 1      allocates 512 TMEM columns; the warp runs the loop and an elected lane issues
+//               tcgen05.mma (M=128, N=256, K=16) with the operands' majorness in the
+//               instruction descriptor;
 //   warps 2..5  epilogue: tcgen05.ld of the 128x256 fp32 accumulator, per-row arithmetic,
 //               16-byte stores.  Two accumulators overlap epilogue and mainloop.
 // Every wait is bounded (globaltimer); on expiry the CTA raises an abort flag, drains, frees
@@ -190,20 +191,21 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const int ntiles = total_tiles(p);
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int s = 0;
-            uint32_t ph = 0;
-            int last_ph[STAGES];
-            for (int i = 0; i < STAGES; i++) last_ph[i] = -1;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const Tile t = decode(p, tile);
-                for (int kb = 0; kb < t.nk; kb++) {
-                    if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
+        // ---------------------------------------------------- TMA producer: the whole warp runs
+        // the loop and the waits, one elected lane issues the copies
+        int s = 0;
+        uint32_t ph = 0;
+        int last_ph[STAGES];
+        for (int i = 0; i < STAGES; i++) last_ph[i] = -1;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const Tile t = decode(p, tile);
+            for (int kb = 0; kb < t.nk; kb++) {
+                if (!waitw(&empty[s], ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
                     const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
                     const uint32_t b_dst = smem_u32(sB + s * B_STAGE);
@@ -235,64 +237,77 @@ tcb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         const int b_n = (rows_mode ? t.g * p.b_rows : 0) + t.nt * BN;
                         tma_load_2d(b_dst, &tmB0, &full[s], b_k, b_n);
                     }
-                    last_ph[s] = (int)ph;
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                }
+                __syncwarp();
+                last_ph[s] = (int)ph;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-            if (!ok) {
-                for (int i = 0; i < STAGES; i++)
-                    if (last_ph[i] >= 0)
-                        wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
-            }
+        }
+        if (!ok && lane == 0) {   // let the copies in flight land before the CTA can exit
+            for (int i = 0; i < STAGES; i++)
+                if (last_ph[i] >= 0)
+                    wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | ((A_MN ? 1u : 0u) << 15) |
-                                       ((B_MN ? 1u : 0u) << 16);
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            int it = 0;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-                const Tile t = decode(p, tile);
-                const int acc = it & 1;
-                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+        // ---------------------------------------------------- MMA issuer: the whole warp runs the
+        // loop and the waits, one elected lane issues the MMAs and commits (one thread issuing
+        // between mbarrier waits spends ~100-115 cycles per MMA); the ring descriptors advance by
+        // adding the stage size to their address field
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | ((A_MN ? 1u : 0u) << 15) |
+                                   ((B_MN ? 1u : 0u) << 16);
+        // K 16 = 32 bytes (K-major) or 2048 bytes (MN-major): +2 or +128 in the address field
+        constexpr uint64_t a_step = A_MN ? 128 : 2, b_step = B_MN ? 128 : 2;
+        const uint64_t ad0 = A_MN ? sw128_mn_desc(smem_u32(sA)) : sw128_desc(smem_u32(sA));
+        const uint64_t bd0 = B_MN ? sw128_mn_desc(smem_u32(sB)) : sw128_desc(smem_u32(sB));
+        uint64_t ad = ad0, bd = bd0;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+            const Tile t = decode(p, tile);
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!waitw(&tempty[acc], aph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < t.nk; kb++) {
+                if (!waitw(&full[s], ph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < t.nk; kb++) {
-                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // descriptors advance by addition: K 16 = 32 bytes (K-major) or 2048 bytes
-                    // (MN-major), i.e. +2 or +128 in the address field
-                    const uint32_t a0 = smem_u32(sA + s * A_STAGE);
-                    const uint32_t b0 = smem_u32(sB + s * B_STAGE);
-                    const uint64_t ad = A_MN ? sw128_mn_desc(a0) : sw128_desc(a0);
-                    const uint64_t bd = B_MN ? sw128_mn_desc(b0) : sw128_desc(b0);
-                    constexpr uint64_t a_step = A_MN ? 128 : 2, b_step = B_MN ? 128 : 2;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; kk++)
                         umma_bf16(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
                                   (kb > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
                 }
-                if (ok) umma_commit(&tfull[acc]);
+                __syncwarp();
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                    ad = ad0;
+                    bd = bd0;
+                } else {
+                    ad += (uint64_t)(A_STAGE >> 4);
+                    bd += (uint64_t)(B_STAGE >> 4);
+                }
             }
+            // after the loop, so that a tile without k-blocks (an empty group) is released too
+            if (ok && elect_one()) umma_commit(&tfull[acc]);
+            __syncwarp();
+        }
+        // every MMA issued by the elected lane completes before TMEM can be released
+        if (elect_one()) {
             umma_commit(drain);
             wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
         }
