@@ -10,10 +10,12 @@
 // tokens for a shared expert); empty groups own no tile.
 //
 // Design (one CTA per SM, persistent, warp-specialised, 192 threads):
-//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128-byte swizzle) per
-//               k-block into a 4-stage shared-memory ring (48 KB per stage);
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
-//               K=16, fp32 accumulate) and frees ring slots with tcgen05.commit;
+//   warp 0      TMA producer (the warp runs the loop, an elected lane issues): A tile 128x64
+//               and B tile 256x64 (bf16, 128-byte swizzle) per k-block into a 4-stage
+//               shared-memory ring (48 KB per stage);
+//   warp 1      allocates 512 TMEM columns; the warp runs the loop and an elected lane issues
+//               tcgen05.mma (M=128, N=256, K=16, fp32 accumulate) and frees ring slots with
+//               tcgen05.commit;
 //   warps 2..5  epilogue: tcgen05.ld of the 128x256 fp32 accumulator (each warp its 32-lane
 //               quarter), silu*mul or scale in fp32, one rounding to bf16, 16-byte stores.
 // Two accumulators (2 x 256 columns) let the epilogue of tile i overlap the mainloop of i+1.
@@ -276,22 +278,23 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int nk = (p.K + BK - 1) / BK;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int s = 0;
-            uint32_t ph = 0;
-            int last_ph[STAGES];
-            for (int i = 0; i < STAGES; i++) last_ph[i] = -1;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile(p, tile);
-                const int a_y = (int)(t.a_row0 + (int64_t)t.mt * BM);
-                const int b_y = t.g * p.b_rows + t.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
-                for (int kb = 0; kb < nk; kb++) {
-                    if (!wait1(&empty[s], ph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
+        // ---------------------------------------------------- TMA producer: the whole warp runs
+        // the loop and the waits, one elected lane issues the copies
+        int s = 0;
+        uint32_t ph = 0;
+        int last_ph[STAGES];
+        for (int i = 0; i < STAGES; i++) last_ph[i] = -1;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const TileInfo t = decode_tile(p, tile);
+            const int a_y = (int)(t.a_row0 + (int64_t)t.mt * BM);
+            const int b_y = t.g * p.b_rows + t.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+            for (int kb = 0; kb < nk; kb++) {
+                if (!waitw(&empty[s], ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
                     const int kx = kb * BK;
                     tma_load_2d(smem_u32(sA + s * A_STAGE), &tmA, &full[s], kx, a_y);
@@ -302,51 +305,54 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     } else {
                         tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB0, &full[s], kx, b_y);
                     }
-                    last_ph[s] = (int)ph;
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                }
+                __syncwarp();
+                last_ph[s] = (int)ph;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-            if (!ok) {
-                // let every copy already issued land before the CTA can exit
-                for (int i = 0; i < STAGES; i++)
-                    if (last_ph[i] >= 0)
-                        wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
-            }
+        }
+        if (!ok && lane == 0) {
+            // let every copy already issued land before the CTA can exit
+            for (int i = 0; i < STAGES; i++)
+                if (last_ph[i] >= 0)
+                    wait1(&full[i], (uint32_t)last_ph[i], abort_flag, kDrainTimeoutNs, false);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            // Kept lean (its issue rate shows in the tensor pipe's utilisation): one k-loop per
-            // tile kind, descriptors advanced by addition (+2 = 32 bytes = K 16).
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            int it = 0;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-                const int acc = it & 1;
-                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-                if (!wait1(&tempty[acc], aph ^ 1u, abort_flag, kWaitTimeoutNs, true)) {
+        // ---------------------------------------------------- MMA issuer: the whole warp runs the
+        // loop and the waits, one elected lane issues the MMAs and commits (one thread issuing
+        // between mbarrier waits spends ~100-115 cycles per MMA); one k-loop per tile kind,
+        // descriptors advanced by addition (+2 = 32 bytes = K 16 within a stage, the stage size
+        // between stages)
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+        uint64_t ad = ad0, bd = bd0;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!waitw(&tempty[acc], aph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            const TileInfo t = decode_tile(p, tile);
+            // swapped: D0 = W[0:128) . A^T and D1 = W[128:256) . A^T, each 128 x n16
+            const uint32_t idesc_sw = idesc_bf16_f32(BM, (t.tr + 15) & ~15);
+            for (int kb = 0; kb < nk; kb++) {
+                if (!waitw(&full[s], ph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const TileInfo t = decode_tile(p, tile);
-                // swapped: D0 = W[0:128) . A^T and D1 = W[128:256) . A^T, each 128 x n16
-                const uint32_t idesc_sw = idesc_bf16_f32(BM, (t.tr + 15) & ~15);
-                for (int kb = 0; kb < nk; kb++) {
-                    if (!wait1(&full[s], ph, abort_flag, kWaitTimeoutNs, true)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t ad = sw128_desc(smem_u32(sA + s * A_STAGE));
-                    const uint64_t bd = sw128_desc(smem_u32(sB + s * B_STAGE));
+                if (elect_one()) {
                     if (!t.swap) {
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; kk++)
@@ -362,14 +368,23 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                     }
                     umma_commit(&empty[s]);
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
                 }
-                if (ok) umma_commit(&tfull[acc]);
+                __syncwarp();
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                    ad = ad0;
+                    bd = bd0;
+                } else {
+                    ad += (uint64_t)(A_STAGE >> 4);
+                    bd += (uint64_t)(B_STAGE >> 4);
+                }
             }
-            // every MMA issued by this thread completes before TMEM can be released
+            if (ok && elect_one()) umma_commit(&tfull[acc]);
+            __syncwarp();
+        }
+        // every MMA issued by the elected lane completes before TMEM can be released
+        if (elect_one()) {
             umma_commit(drain);
             wait1(drain, 0, abort_flag, kDrainTimeoutNs, false);
         }

@@ -295,7 +295,9 @@ router_tiled_kernel(const T* __restrict__ x, const float* __restrict__ W_r,
 
 // P_sum[e] = sum over router blocks b of p_part[b][e], in a fixed order (deterministic): one
 // block of 32 warps per 32 experts, lane = expert (coalesced rows); warp w adds blocks w, w + 32,
-// ... in order with eight loads in flight, then warp 0 adds the 32 warp sums in warp order.
+// ... in order, then warp 0 adds the 32 warp sums in warp order.  Only E / 32 blocks run, so the
+// kernel is bound by load latency: each warp keeps 32 loads in flight (8 took 8 us on 2048
+// partial rows, four rounds of latency).
 __global__ void __launch_bounds__(1024) reduce_p_kernel(const float* __restrict__ p_part, int blocks,
                                                         int E, float* __restrict__ P_sum) {
     __shared__ float part[32][33];
@@ -303,13 +305,14 @@ __global__ void __launch_bounds__(1024) reduce_p_kernel(const float* __restrict_
     const int e = blockIdx.x * 32 + lane;
     float s = 0.f;
     if (e < E) {
+        constexpr int kInFlight = 32;
         int b = warp;
-        for (; b + 7 * 32 < blocks; b += 8 * 32) {
-            float v[8];
+        for (; b + (kInFlight - 1) * 32 < blocks; b += kInFlight * 32) {
+            float v[kInFlight];
 #pragma unroll
-            for (int i = 0; i < 8; i++) v[i] = p_part[(int64_t)(b + 32 * i) * E + e];
+            for (int i = 0; i < kInFlight; i++) v[i] = p_part[(int64_t)(b + 32 * i) * E + e];
 #pragma unroll
-            for (int i = 0; i < 8; i++) s += v[i];
+            for (int i = 0; i < kInFlight; i++) s += v[i];
         }
         for (; b < blocks; b += 32) s += p_part[(int64_t)b * E + e];
     }
