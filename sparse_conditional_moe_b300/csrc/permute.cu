@@ -53,20 +53,38 @@ __device__ __forceinline__ int warp_slots(int64_t A, int64_t* f0) {
     return spw;
 }
 
-// Per-warp expert counts of the warp's slots into cnt[warp][e] (E entries per warp).
-__device__ __forceinline__ void warp_count(const int32_t* __restrict__ idx, int64_t A, int E,
-                                           int64_t f_begin, int spw, int* cnt_row, int32_t* err) {
+// The expert of each of the warp's slots, all steps loaded at once (the loads' latency is
+// paid once, not once per step): ev[step] for slot f_begin + 32 step + lane, -1 past A or for
+// an index outside [0, E) (reported when err is given).
+constexpr int kPermSteps = kPermSlotsPerWarp / 32;
+__device__ __forceinline__ void load_slots(const int32_t* __restrict__ idx, int64_t A, int E,
+                                           int64_t f_begin, int spw, int (&ev)[kPermSteps],
+                                           int32_t* err) {
     const int lane = threadIdx.x & 31;
-    for (int step = 0; step < spw / 32; step++) {
-        int64_t f = f_begin + step * 32 + lane;
-        int e = -1;
-        if (f < A) {
-            e = idx[f];
-            if (e < 0 || e >= E) {
-                set_err(err, MOE_DEVERR_BOUNDS);
-                e = -1;
-            }
+#pragma unroll
+    for (int step = 0; step < kPermSteps; step++) {
+        const int64_t f = f_begin + step * 32 + lane;
+        ev[step] = (step < spw / 32 && f < A) ? idx[f] : 0;
+    }
+#pragma unroll
+    for (int step = 0; step < kPermSteps; step++) {
+        const int64_t f = f_begin + step * 32 + lane;
+        if (!(step < spw / 32 && f < A)) {
+            ev[step] = -1;
+        } else if (ev[step] < 0 || ev[step] >= E) {
+            if (err) set_err(err, MOE_DEVERR_BOUNDS);
+            ev[step] = -1;
         }
+    }
+}
+
+// Per-warp expert counts of the warp's slots into cnt[warp][e] (E entries per warp).
+__device__ __forceinline__ void warp_count(const int (&ev)[kPermSteps], int spw, int* cnt_row) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int step = 0; step < kPermSteps; step++) {
+        if (step >= spw / 32) break;
+        const int e = ev[step];
         unsigned mask = __match_any_sync(0xffffffffu, e);
         int leader = __ffs(mask) - 1;
         if (e >= 0 && lane == leader) cnt_row[e] += __popc(mask);
@@ -83,7 +101,9 @@ perm_count_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __
     __syncthreads();
     int64_t f0 = 0;
     const int spw = warp_slots(A, &f0);
-    warp_count(idx, A, E, f0, spw, cnt + warp * E, err);
+    int ev[kPermSteps];
+    load_slots(idx, A, E, f0, spw, ev, err);
+    warp_count(ev, spw, cnt + warp * E);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kPermThreads) {
         int s = 0;
@@ -153,10 +173,12 @@ perm_scan_kernel(const int32_t* __restrict__ blk_hist, int blocks, int E, int64_
     }
 }
 
-// Scatter of this block's slots given the per-warp run bases in cnt[warp][e] and the offsets,
-// kept counts and kept offsets per expert (shared by perm_scatter_kernel and perm_fused_kernel).
-__device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ idx,
-                                              const float* __restrict__ w, int64_t A, int k, int E,
+// Scatter of this block's slots (their experts ev from load_slots) given the per-warp run bases
+// in cnt[warp][e] and the offsets, kept counts and kept offsets per expert (shared by
+// perm_scatter_kernel and perm_fused_kernel).  The slots' routing weights are loaded up front
+// like their experts.
+__device__ __forceinline__ void scatter_slots(const int (&ev)[kPermSteps],
+                                              const float* __restrict__ w, int64_t A, int k,
                                               int64_t f0, int spw, int* base,
                                               const int32_t* offsets, const int32_t* kept,
                                               const int32_t* kept_off, int32_t* __restrict__ perm,
@@ -165,13 +187,17 @@ __device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ idx,
                                               float* __restrict__ row_weight) {
     const int lane = threadIdx.x & 31;
     const unsigned lt = (1u << lane) - 1u;
-    for (int step = 0; step < spw / 32; step++) {
-        int64_t f = f0 + step * 32 + lane;
-        int e = -1;
-        if (f < A) {
-            e = idx[f];
-            if (e < 0 || e >= E) e = -1;
-        }
+    float wv[kPermSteps];
+#pragma unroll
+    for (int step = 0; step < kPermSteps; step++) {
+        const int64_t f = f0 + step * 32 + lane;
+        wv[step] = (w && step < spw / 32 && f < A) ? w[f] : 1.f;
+    }
+#pragma unroll
+    for (int step = 0; step < kPermSteps; step++) {
+        if (step >= spw / 32) break;
+        const int64_t f = f0 + step * 32 + lane;
+        const int e = ev[step];
         unsigned mask = __match_any_sync(0xffffffffu, e);
         int r = 0;
         if (e >= 0) r = base[e] + __popc(mask & lt);
@@ -185,7 +211,7 @@ __device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ idx,
                     int p = kept_off[e] + r;
                     pos[f] = p;
                     row_token[p] = (int32_t)(f / k);
-                    row_weight[p] = w ? w[f] : 1.f;
+                    row_weight[p] = wv[step];
                 } else {
                     pos[f] = -1;
                 }
@@ -208,7 +234,9 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w
     __syncthreads();
     int64_t f0 = 0;
     const int spw = warp_slots(A, &f0);
-    warp_count(idx, A, E, f0, spw, cnt + warp * E, nullptr);
+    int ev[kPermSteps];
+    load_slots(idx, A, E, f0, spw, ev, nullptr);
+    warp_count(ev, spw, cnt + warp * E);
     __syncthreads();
     // per expert: exclusive scan over warps, starting at this block's base
     for (int e = threadIdx.x; e < E; e += kPermThreads) {
@@ -220,7 +248,7 @@ perm_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w
         }
     }
     __syncthreads();
-    scatter_slots(idx, w, A, k, E, f0, spw, cnt + warp * E, offsets, kept, kept_off, perm, pos,
+    scatter_slots(ev, w, A, k, f0, spw, cnt + warp * E, offsets, kept, kept_off, perm, pos,
                   row_token, row_weight);
 }
 
@@ -245,7 +273,9 @@ perm_fused_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, 
     __syncthreads();
     int64_t f0 = 0;
     const int spw = warp_slots(A, &f0);
-    warp_count(idx, A, E, f0, spw, cnt + warp * E, err);
+    int ev[kPermSteps];   // kept in registers across the grid barrier for the scatter
+    load_slots(idx, A, E, f0, spw, ev, err);
+    warp_count(ev, spw, cnt + warp * E);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kPermThreads) {
         int sum = 0;
@@ -260,8 +290,19 @@ perm_fused_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, 
     const int e_lo = min(E, (int)threadIdx.x * per), e_hi = min(E, e_lo + per);
     int loc_c = 0, loc_k = 0;
     for (int e = e_lo; e < e_hi; e++) {
-        int before = 0, total = 0;
-        for (int b = 0; b < nb; b++) {
+        // sixteen loads in flight: the histogram's rows are read in rounds, not one by one
+        int before = 0, total = 0, b = 0;
+        for (; b + 16 <= nb; b += 16) {
+            int h[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) h[i] = __ldcg(blk_hist + (int64_t)(b + i) * E + e);
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                if (b + i < (int)blockIdx.x) before += h[i];
+                total += h[i];
+            }
+        }
+        for (; b < nb; b++) {
             const int h = __ldcg(blk_hist + (int64_t)b * E + e);
             if (b < (int)blockIdx.x) before += h;
             total += h;
@@ -307,7 +348,7 @@ perm_fused_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, 
         }
     }
     __syncthreads();
-    scatter_slots(idx, w, A, k, E, f0, spw, cnt + warp * E, s_off, s_kept, s_koff, perm, pos,
+    scatter_slots(ev, w, A, k, f0, spw, cnt + warp * E, s_off, s_kept, s_koff, perm, pos,
                   row_token, row_weight);
 }
 
