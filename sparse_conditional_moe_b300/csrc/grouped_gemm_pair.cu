@@ -122,6 +122,7 @@ struct PairParams {
 
 struct PTile {
     int g, c, w;
+    int nch;           // chunks of the group (how many tiles read each of its weight tiles)
     int rows;          // token rows of this chunk (1..256)
     int n_mma;         // rows rounded up to 16
     int box;           // token box index: tok_box_rows(box) rows per CTA
@@ -185,6 +186,7 @@ __device__ __forceinline__ PTile decode_tile(const PairParams& p, int tile, int 
         local = tile - off0 * p.n_wt;
     }
     raster_tile(local, nch, p.n_wt, t.c, t.w);
+    t.nch = nch;
     // the group's rows split evenly over its chunks: the first n % nch chunks get one more
     const int base = n / nch, rem = n - base * nch;
     t.rows = base + (t.c < rem ? 1 : 0);
@@ -322,6 +324,13 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
         int s = 0, qs = 0;
         uint32_t ph = 0, qph = 0;
         bool ok = true;
+        // A chunk's token rows are re-read by every weight tile of its group, a weight tile by
+        // the group's other chunks only.  For gate/up tiles of groups of at most two chunks the
+        // weights are marked evict-first, so that the token rows stay in L2.  Groups of more
+        // chunks (the Mixtral-shaped layer's four) re-read each weight tile too often for that,
+        // and the down GEMM keeps the default policy: evict-first weights there slowed it and
+        // the combine that reads its output.
+        const uint64_t w_policy = policy_evict_first();
         while (ok) {
             PTile t;
             const int got = pop_tile(tq, q_full, q_empty, qs, qph, t, abort_flag);
@@ -347,8 +356,13 @@ pair_grouped_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_const
                     const int kx = kb * BK;
                     if (wts) {
                         const uint32_t a = smem_u32(sA + s * A_STAGE);
-                        tma_load_2d_pair(a, &tmW0, fb, kx, wy);
-                        if (EPI == EPI_SWIGLU) tma_load_2d_pair(a + A_STAGE / 2, &tmW1, fb, kx, wy);
+                        if (EPI == EPI_SWIGLU && t.nch <= 2) {
+                            tma_load_2d_pair_hint(a, &tmW0, fb, kx, wy, w_policy);
+                            tma_load_2d_pair_hint(a + A_STAGE / 2, &tmW1, fb, kx, wy, w_policy);
+                        } else {
+                            tma_load_2d_pair(a, &tmW0, fb, kx, wy);
+                            if (EPI == EPI_SWIGLU) tma_load_2d_pair(a + A_STAGE / 2, &tmW1, fb, kx, wy);
+                        }
                     } else {
                         tma_load_2d_pair(smem_u32(sB + s * B_STAGE), mt, fb, kx, tok_y);
                     }
